@@ -1,0 +1,28 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA library)")
+    config.addinivalue_line("markers", "slow: full-size workload")
+
+
+def golden(name):
+    return os.path.join(ROOT, "tests", "golden", name)
+
+
+def read_constants():
+    out = {}
+    with open(golden("paper_constants.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                out[k] = float(v)
+    return out
