@@ -359,6 +359,16 @@ int or_topk_f32(const float *scores, const int32_t *pos, int64_t n, int k, int32
 /* Hierarchical candidate pool  [Notes] section 3, [Summary] item 3           */
 /* ------------------------------------------------------------------------ */
 
+/* Block maxima: max score over the visible entries of each aligned 8-entry block. */
+void or_blockmax(const double *scores, int64_t n, double *out)
+{
+    for (int64_t b = 0; b < (n + 7) / 8; ++b) {
+        double m = -INFINITY;
+        for (int64_t j = 8 * b; j < 8 * b + 8 && j < n; ++j) m = fmax(m, scores[j]);
+        out[b] = m;
+    }
+}
+
 /* Block score = max token score over the visible entries of each aligned
  * 8-entry block; the top nblk_max blocks (ties to the lower block) form the
  * pool.  blk_out gets the chosen block ids ascending; returns the number of
@@ -367,11 +377,7 @@ int or_pool(const double *scores, int64_t n, int nblk_max, int32_t *blk_out, int
 {
     int64_t nb = (n + 7) / 8;
     double *bm = (double *)malloc(sizeof(double) * (nb > 0 ? nb : 1));
-    for (int64_t b = 0; b < nb; ++b) {
-        double m = -INFINITY;
-        for (int64_t j = 8 * b; j < 8 * b + 8 && j < n; ++j) m = fmax(m, scores[j]);
-        bm[b] = m;
-    }
+    or_blockmax(scores, n, bm);
     int c = or_topk(bm, NULL, nb, nblk_max, blk_out);
     free(bm);
     *nblk = c;
@@ -381,16 +387,6 @@ int or_pool(const double *scores, int64_t n, int nblk_max, int32_t *blk_out, int
         pool_n += (int)(hi - lo);
     }
     return pool_n;
-}
-
-/* Block maxima only (for comparing the indexer's block-max output). */
-void or_blockmax(const double *scores, int64_t n, double *out)
-{
-    for (int64_t b = 0; b < (n + 7) / 8; ++b) {
-        double m = -INFINITY;
-        for (int64_t j = 8 * b; j < 8 * b + 8 && j < n; ++j) m = fmax(m, scores[j]);
-        out[b] = m;
-    }
 }
 
 /* ------------------------------------------------------------------------ */

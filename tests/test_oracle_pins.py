@@ -352,6 +352,19 @@ def test_pool_size_at_1m_is_paper_figure():
     assert np.array_equal(blk, np.sort(np.lexsort((np.arange(len(bm)), -bm))[:2048]))
 
 
+def test_pool_partial_last_block():
+    # the block holding the newest entries may be partial: only its visible
+    # entries score it and count towards the pool
+    rng = np.random.default_rng(79)
+    n = 8 * 3000 + 3
+    sc = rng.normal(size=n)
+    sc[-3:] = 50.0                                    # make the partial block a winner
+    blk, pn = O.pool(sc, 2048)
+    pad = np.concatenate([sc, np.full(5, -np.inf)]).reshape(-1, 8).max(1)
+    assert np.array_equal(blk, np.sort(np.lexsort((np.arange(len(pad)), -pad))[:2048]))
+    assert blk[-1] == n // 8 and pn == 8 * 2047 + 3
+
+
 def _cache_from_latents(rng, n, d_idx, exact=False):
     C = rng.normal(size=(1, n, 512)).astype(np.float32)
     if exact:
