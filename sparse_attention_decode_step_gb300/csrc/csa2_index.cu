@@ -1,0 +1,542 @@
+// csa2_index.cu -- indexer scoring (Full and Reindex modes) on tcgen05.
+//
+// score(q, j) = sum_h w_h * ReLU(q_h . k_j), q_h and k_j in E4M3 with
+// power-of-two scales ([Notes] section 2: Full mode scores the whole visible
+// context and Reindex rescores a shared key with its own query; section 3:
+// the block-max pool and the Reindex search inside it).
+//
+// Layout of the contraction (swap-AB): the M = 128 rows of one MMA are 128
+// cache entries (a TMA-loaded tile of the FP8 key cache, K-major, 128-byte
+// swizzle), the N columns are the indexer heads of one query group (group *
+// h_idx rows of FP8 query, padded to a multiple of 16) and K = d_idx.  The
+// accumulator (128 lanes x N fp32) lives in tensor memory; each epilogue
+// thread owns one entry (one TMEM lane) and turns its N dot products into
+// `group` scores with the ReLU-weighted head sum, then reduces 8 lanes for the
+// block max.  At decode the kernel is bound by the key stream from HBM
+// (132 B per entry), so the pipeline is built to keep ~128 KB of TMA loads in
+// flight per SM; at prefill (group 32, N = 256) it is bound by the FP8 MMA.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
+// Units of work are (query group, 128-entry tile); each CTA takes a contiguous
+// range of units so the query tile (B operand) is reloaded only when the group
+// changes.  Every wait is bounded (csa2::kSpinLimit) and sets an abort flag.
+#include "csa2_device.cuh"
+#include "csa2_internal.h"
+
+namespace csa2 {
+
+constexpr int kIdxThreads = 192;
+constexpr int kTile = 128;
+
+struct IndexParams {
+    const float *kscale;
+    const int64_t *seq_base;
+    const int32_t *seq_len;
+    int64_t cap;
+    int batch, d_idx, m;
+    const int32_t *q_seq, *q_pos;
+    const float *q_idx, *w;
+    int nq, group, n_groups, h_idx, n_pad;
+    int64_t max_n;
+    // reindex (pool_blk != nullptr)
+    const int32_t *pool_blk, *pool_n;
+    int pool_blocks;
+    // workspace
+    uint8_t *q8img;    // [n_groups][n_pad][d_idx], swizzled like the smem tile
+    float *ws;         // [nq][h_idx] = w * q scale
+    int32_t *nt;       // [nq] candidates of each query
+    int32_t *gtiles;   // [n_groups] tiles of each group
+    // outputs
+    float *scores;
+    int64_t ld;
+    float *blockmax;
+    int64_t ld_bm;
+    int32_t *n_valid;
+    uint32_t *counters;
+};
+
+// Byte offset of (row r, byte c) in a K-major tile with `rowb`-byte rows under
+// the matching TMA/UMMA swizzle (128 B rows: SW128, 64 B rows: SW64).
+__device__ __forceinline__ uint32_t swz_off(uint32_t r, uint32_t c, uint32_t rowb)
+{
+    uint32_t chunk = c >> 4;
+    uint32_t x = (rowb == 128) ? (r & 7u) : ((r >> 1) & 3u);
+    return r * rowb + ((chunk ^ x) << 4) + (c & 15u);
+}
+
+// ---------------------------------------------------------------- prologue
+// One CTA per query group: candidate counts, tiles per group, the FP8 query
+// image (the smem B operand, pre-swizzled) and w * q scale.
+__global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
+{
+    const int g = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q0 = g * p.group;
+    __shared__ int s_bad;
+    __shared__ int s_maxn;
+    if (threadIdx.x == 0) { s_bad = 0; s_maxn = 0; }
+    __syncthreads();
+    const int b = p.q_seq[q0];   // validated per query below before any use
+    if (threadIdx.x < p.group) {
+        const int q = q0 + threadIdx.x;
+        int bad = 0;
+        int64_t n = 0;
+        if (p.q_seq[q] != b || b < 0 || b >= p.batch) bad = 1;
+        if (!bad) {
+            const int64_t base = p.seq_base[b];
+            const int64_t room = p.seq_base[b + 1] - base;
+            const int64_t len = p.seq_len[b];
+            if ((base & 7) != 0 || base + room > p.cap || len > room) bad = 1;
+            if (p.pool_blk == nullptr) {
+                n = ((int64_t)p.q_pos[q] + 1) / p.m;
+                if (n > len || n > p.max_n || p.q_pos[q] < 0) { bad = 1; n = 0; }
+            } else {
+                n = p.pool_n[q];
+                if (n < 0 || n > 8LL * p.pool_blocks) { bad = 1; n = 0; }
+            }
+        }
+        if (bad) { atomicOr(&s_bad, 1); n = 0; }
+        p.nt[q] = (int32_t)n;
+        if (p.n_valid) p.n_valid[q] = (int32_t)n;
+        atomicMax(&s_maxn, (int)n);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (s_bad) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+        p.gtiles[g] = s_bad ? 0 : (s_maxn + kTile - 1) / kTile;
+    }
+    // FP8 query rows: row r = (query in group) * h_idx + head; padding rows = 0
+    uint8_t *img = p.q8img + (int64_t)g * p.n_pad * p.d_idx;
+    for (int r = warp; r < p.n_pad; r += blockDim.x / 32) {
+        const int qq = r / p.h_idx, h = r % p.h_idx;
+        const bool real = qq < p.group;
+        const float *src = p.q_idx + ((int64_t)(q0 + qq) * p.h_idx + h) * p.d_idx;
+        if (p.d_idx == 128) {
+            float4 v = real ? __ldg(reinterpret_cast<const float4 *>(src) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float s = fp8_pow2_scale(a);
+            uint32_t word = e4m3_byte(v.x / s) | (e4m3_byte(v.y / s) << 8) |
+                            (e4m3_byte(v.z / s) << 16) | (e4m3_byte(v.w / s) << 24);
+            *reinterpret_cast<uint32_t *>(img + swz_off(r, lane * 4, 128)) = word;
+            if (real && lane == 0) p.ws[(int64_t)(q0 + qq) * p.h_idx + h] =
+                __ldg(p.w + (int64_t)(q0 + qq) * p.h_idx + h) * s;
+        } else {
+            float2 v = real ? __ldg(reinterpret_cast<const float2 *>(src) + lane)
+                            : make_float2(0.f, 0.f);
+            float a = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float s = fp8_pow2_scale(a);
+            uint16_t word = (uint16_t)(e4m3_byte(v.x / s) | (e4m3_byte(v.y / s) << 8));
+            *reinterpret_cast<uint16_t *>(img + swz_off(r, lane * 2, 64)) = word;
+            if (real && lane == 0) p.ws[(int64_t)(q0 + qq) * p.h_idx + h] =
+                __ldg(p.w + (int64_t)(q0 + qq) * p.h_idx + h) * s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+struct UnitIter {
+    int g, t;
+    int64_t u, u1;
+};
+
+__device__ __forceinline__ void unit_next(UnitIter &it, const int32_t *gtiles, int n_groups)
+{
+    ++it.u;
+    ++it.t;
+    while (it.g < n_groups && it.t >= gtiles[it.g]) { ++it.g; it.t = 0; }
+}
+
+template <int D_IDX>
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    index_main_kernel(const __grid_constant__ CUtensorMap tmap, IndexParams p, int stages, int nacc)
+{
+    constexpr uint32_t kABytes = kTile * D_IDX;
+    constexpr uint32_t kSbo = 8 * D_IDX;
+    constexpr uint32_t kLayout = (D_IDX == 128) ? kLayoutSW128 : kLayoutSW64;
+    const uint32_t b_bytes = (uint32_t)p.n_pad * D_IDX;
+    const uint32_t b_stride = (b_bytes + 1023u) & ~1023u;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~(uintptr_t)1023);
+    uint8_t *sA = smem;                                      // stages x kABytes
+    float *sK = reinterpret_cast<float *>(sA + stages * kABytes);     // stages x 128 key scales
+    uint8_t *sB = reinterpret_cast<uint8_t *>(sK + stages * kTile);   // 2 x b_stride (1024-aligned)
+    sB = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sB) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + 2 * b_stride);
+    uint64_t *full = bars, *empty = bars + stages;
+    uint64_t *bfull = empty + stages, *bempty = bfull + 2;
+    uint64_t *tfull = bempty + 2, *tempty = tfull + nacc;
+    uint64_t *done = tempty + nacc;
+    int *sI = reinterpret_cast<int *>(done + 1);             // misc ints
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sI + 8);
+    int64_t *s_scan = reinterpret_cast<int64_t *>(s_tmem + 2);  // kIdxThreads
+
+    volatile int *abort_flag = sI;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t ncols_acc = (uint32_t)p.n_pad;
+    uint32_t tm_cols = 32;
+    while (tm_cols < ncols_acc * nacc) tm_cols <<= 1;
+
+    if (tid == 0) {
+        sI[0] = 0;
+        for (int s = 0; s < stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&bfull[i], 1); mbar_init(&bempty[i], 1); }
+        for (int i = 0; i < nacc; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 4); }
+        mbar_init(done, 1);
+        fence_barrier_init();
+        prefetch_tmap(&tmap);
+    }
+    if (warp == 1) { tmem_alloc(s_tmem, tm_cols); tmem_relinquish(); }
+
+    // ---- this CTA's unit range [u0, u1) and its first (group, tile)
+    {
+        const int per = (p.n_groups + kIdxThreads - 1) / kIdxThreads;
+        const int gs = min(tid * per, p.n_groups), ge = min(gs + per, p.n_groups);
+        int64_t mine = 0;
+        for (int g = gs; g < ge; ++g) mine += p.gtiles[g];
+        s_scan[tid] = mine;
+        __syncthreads();
+        if (tid == 0) {
+            int64_t acc = 0;
+            for (int i = 0; i < kIdxThreads; ++i) { int64_t v = s_scan[i]; s_scan[i] = acc; acc += v; }
+            const int64_t T = acc;
+            const int64_t u0 = T * blockIdx.x / gridDim.x, u1 = T * (blockIdx.x + 1) / gridDim.x;
+            reinterpret_cast<int64_t *>(sI + 2)[0] = u0;
+            reinterpret_cast<int64_t *>(sI + 2)[1] = u1;
+            sI[1] = p.n_groups;   // start group (n_groups = none)
+            sI[6] = 0;
+        }
+        __syncthreads();
+        const int64_t u0 = reinterpret_cast<int64_t *>(sI + 2)[0];
+        const int64_t u1 = reinterpret_cast<int64_t *>(sI + 2)[1];
+        int64_t acc = s_scan[tid];
+        if (u0 < u1 && acc <= u0 && u0 < acc + mine) {
+            for (int g = gs; g < ge; ++g) {
+                const int64_t n = p.gtiles[g];
+                if (u0 < acc + n) { sI[1] = g; sI[6] = (int)(u0 - acc); break; }
+                acc += n;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    UnitIter it0;
+    it0.g = sI[1];
+    it0.t = sI[6];
+    it0.u = reinterpret_cast<int64_t *>(sI + 2)[0];
+    it0.u1 = reinterpret_cast<int64_t *>(sI + 2)[1];
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0 && it0.u < it0.u1) {
+            UnitIter it = it0;
+            int stage = 0;
+            uint32_t phase = 0;
+            int prev_g = -1, bidx = 1;
+            uint32_t buse[2] = {0, 0};
+            uint32_t armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // stages <= 8
+            while (it.u < it.u1) {
+                const int g = it.g, t = it.t;
+                const int q0 = g * p.group;
+                const int b = p.q_seq[q0];
+                const int64_t base = p.seq_base[b];
+                if (g != prev_g) {
+                    bidx ^= 1;
+                    if (!mbar_wait(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)) break;
+                    ++buse[bidx];
+                    mbar_arrive_expect_tx(&bfull[bidx], b_bytes);
+                    bulk_load(sB + bidx * b_stride, p.q8img + (int64_t)g * b_bytes, b_bytes,
+                              &bfull[bidx]);
+                    prev_g = g;
+                }
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) break;
+                uint8_t *dstA = sA + stage * kABytes;
+                float *dstK = sK + stage * kTile;
+                if (p.pool_blk == nullptr) {
+                    const int64_t r0 = base + (int64_t)t * kTile;
+                    int64_t nk = p.cap - r0;
+                    nk = nk > kTile ? kTile : nk;               // cap % 8 == 0, r0 % 8 == 0
+                    mbar_arrive_expect_tx(&full[stage], kABytes + (uint32_t)nk * 4u);
+                    tma_load_2d(dstA, &tmap, 0, (int32_t)r0, &full[stage]);
+                    bulk_load(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage]);
+                } else {
+                    const int q = q0;   // group == 1 in Reindex mode
+                    const int pn = p.nt[q];
+                    const int nblk = (pn + 7) / 8;
+                    const int bb0 = t * (kTile / 8);
+                    const int nb = min(kTile / 8, nblk - bb0);
+                    const int64_t room = p.seq_base[b + 1] - base;
+                    int nvalid = 0;
+                    for (int i = 0; i < nb; ++i) {
+                        const int blk = p.pool_blk[(int64_t)q * p.pool_blocks + bb0 + i];
+                        if (blk >= 0 && 8LL * blk + 8 <= room) ++nvalid;
+                    }
+                    if (nvalid < nb) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)nvalid * (8u * D_IDX + 32u));
+                    for (int i = 0; i < nb; ++i) {
+                        const int blk = p.pool_blk[(int64_t)q * p.pool_blocks + bb0 + i];
+                        if (blk < 0 || 8LL * blk + 8 > room) continue;
+                        const int64_t r = base + 8LL * blk;
+                        tma_load_2d(dstA + i * 8 * D_IDX, &tmap, 0, (int32_t)r, &full[stage]);
+                        bulk_load(dstK + i * 8, p.kscale + r, 32u, &full[stage]);
+                    }
+                }
+                ++armed[stage];
+                if (++stage == stages) { stage = 0; phase ^= 1u; }
+                unit_next(it, p.gtiles, p.n_groups);
+            }
+            if (it.u < it.u1) { *abort_flag = 1; count_event(p.counters, CSA2_CNT_TIMEOUT); }
+            // no copy of ours may still be landing when the CTA exits: wait (bounded)
+            // for the last arming of every stage and query buffer
+            volatile int no_abort = 0;
+            for (int s = 0; s < stages; ++s)
+                if (armed[s]) mbar_wait(&full[s], (armed[s] - 1u) & 1u, &no_abort);
+            for (int i = 0; i < 2; ++i)
+                if (buse[i]) mbar_wait(&bfull[i], (buse[i] - 1u) & 1u, &no_abort);
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0 && it0.u < it0.u1) {
+            UnitIter it = it0;
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            int prev_g = -1, bidx = 1;
+            uint32_t buse[2] = {0, 0};
+            const uint32_t idesc = instr_desc(128, (uint32_t)p.n_pad, 0, 0, 0, 0);
+            while (it.u < it.u1) {
+                const int g = it.g;
+                if (g != prev_g) {
+                    if (prev_g >= 0) mma_commit(&bempty[bidx]);
+                    bidx ^= 1;
+                    if (!mbar_wait(&bfull[bidx], buse[bidx] & 1u, abort_flag)) break;
+                    ++buse[bidx];
+                    prev_g = g;
+                }
+                if (!mbar_wait(&full[stage], phase, abort_flag)) break;
+                if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + stage * kABytes);
+                const uint32_t b0 = smem_u32(sB + bidx * b_stride);
+                const uint32_t d = tmem_base + (uint32_t)acc * ncols_acc;
+#pragma unroll
+                for (int k = 0; k < D_IDX / 32; ++k) {
+                    mma_f8f6f4(d, smem_desc(a0 + 32 * k, 16, kSbo, kLayout),
+                               smem_desc(b0 + 32 * k, 16, kSbo, kLayout), idesc, k > 0);
+                }
+                mma_commit(&empty[stage]);
+                mma_commit(&tfull[acc]);
+                if (++stage == stages) { stage = 0; phase ^= 1u; }
+                if (++acc == nacc) { acc = 0; aphase ^= 1u; }
+                unit_next(it, p.gtiles, p.n_groups);
+            }
+            if (it.u < it.u1) { *abort_flag = 1; count_event(p.counters, CSA2_CNT_TIMEOUT); }
+            // all MMAs of this thread complete before TMEM is released
+            mma_commit(done);
+            if (!mbar_wait(done, 0, abort_flag)) count_event(p.counters, CSA2_CNT_TIMEOUT);
+        }
+    } else {
+        // ================================================= epilogue (128 threads)
+        const uint32_t quarter = (uint32_t)(warp & 3);
+        const int row = (int)(quarter * 32 + lane);        // TMEM lane = entry within tile
+        UnitIter it = it0;
+        int stage = 0, acc = 0;
+        uint32_t aphase = 0, sphase = 0;
+        int prev_g = -1;
+        float wsr[16];
+        int ntq = 0;
+        while (it.u < it.u1) {
+            const int g = it.g, t = it.t;
+            const int q0 = g * p.group;
+            if (g != prev_g && p.group == 1) {
+                for (int h = 0; h < 16; ++h) wsr[h] = (h < p.h_idx) ? p.ws[(int64_t)q0 * p.h_idx + h] : 0.f;
+                ntq = p.nt[q0];
+                prev_g = g;
+            }
+            // warp-uniform waits: the TMEM loads below are .sync.aligned
+            bool ok = mbar_wait(&tfull[acc], aphase, abort_flag);
+            // the stage's TMA data (key scales) is complete: observe it directly
+            // (already complete, and it cannot be re-armed before this warp releases it)
+            ok = ok && mbar_wait(&full[stage], sphase, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                *abort_flag = 1;
+                if (lane == 0) count_event(p.counters, CSA2_CNT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int64_t j = (int64_t)t * kTile + row;
+            const float sk = sK[stage * kTile + row];
+            const uint32_t tbase = tmem_base + ((quarter * 32u) << 16) + (uint32_t)acc * ncols_acc;
+            if (p.group == 1) {
+                float v[16];
+                tmem_ld16(tbase, v);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+                float s = 0.f;
+#pragma unroll
+                for (int h = 0; h < 16; ++h) s = fmaf(wsr[h], fmaxf(v[h], 0.f), s);
+                s *= sk;
+                const bool valid = j < ntq;
+                if (valid) p.scores[(int64_t)q0 * p.ld + j] = s;
+                if (p.blockmax != nullptr) {
+                    float bm = valid ? s : -INFINITY;
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                    if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q0 * p.ld_bm + (j >> 3)] = bm;
+                }
+            } else {
+                // group of queries: h_idx columns per query, 16 columns per load
+                const int hq = p.h_idx;
+                for (int c0 = 0; c0 < p.group * hq; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + (uint32_t)c0, v);
+                    tmem_wait_ld();
+                    // columns c0..c0+15 cover queries c0/hq .. (c0+15)/hq (hq divides 16 or 16 divides hq)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
+                    if (hq <= 16) {
+                        const int per = 16 / hq;
+                        for (int k2 = 0; k2 < per; ++k2) {
+                            const int qq = c0 / hq + k2;
+                            if (qq >= p.group) break;
+                            const int q = q0 + qq;
+                            const float *wq = p.ws + (int64_t)q * hq;
+                            float s = 0.f;
+                            for (int h = 0; h < hq; ++h) s = fmaf(__ldg(wq + h), v[k2 * hq + h], s);
+                            s *= sk;
+                            const bool valid = j < __ldg(p.nt + q);
+                            if (valid) p.scores[(int64_t)q * p.ld + j] = s;
+                            if (p.blockmax != nullptr) {
+                                float bm = valid ? s : -INFINITY;
+                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                                if ((lane & 7) == 0 && valid)
+                                    p.blockmax[(int64_t)q * p.ld_bm + (j >> 3)] = bm;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            // this warp is done with the stage's key scales: its share of the release
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == stages) { stage = 0; sphase ^= 1u; }
+            if (++acc == nacc) { acc = 0; aphase ^= 1u; }
+            unit_next(it, p.gtiles, p.n_groups);
+        }
+        if (it.u < it.u1) *abort_flag = 1;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tm_cols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+static size_t index_smem_bytes(int d_idx, int n_pad, int stages, int nacc)
+{
+    const size_t a = (size_t)stages * kTile * d_idx;
+    const size_t k = (size_t)stages * kTile * 4;
+    const size_t b = 2 * (((size_t)n_pad * d_idx + 1023) & ~(size_t)1023);
+    const size_t bars = (size_t)(2 * stages + 4 + 2 * nacc + 1) * 8;
+    return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreads * 8;
+}
+
+size_t index_workspace_bytes(int nq, int group, int h_idx, int d_idx)
+{
+    const int n_groups = nq / group;
+    int n_pad = ((group * h_idx + 15) / 16) * 16;
+    size_t s = align_up((size_t)n_groups * n_pad * d_idx, 256);
+    s += align_up((size_t)nq * h_idx * 4, 256);
+    s += align_up((size_t)nq * 4, 256);
+    s += align_up((size_t)n_groups * 4, 256);
+    return s;
+}
+
+cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const float *q_idx,
+                         const float *w, int h_idx, int64_t max_n, const int32_t *pool_blk,
+                         const int32_t *pool_n, int pool_blocks, float *scores, int64_t ld,
+                         float *blockmax, int64_t ld_bm, int32_t *n_valid, void *ws,
+                         uint32_t *counters, cudaStream_t st)
+{
+    IndexParams p{};
+    p.kscale = c.kscale;
+    p.seq_base = c.seq_base;
+    p.seq_len = c.seq_len;
+    p.cap = c.cap;
+    p.batch = c.batch;
+    p.d_idx = c.d_idx;
+    p.m = c.m;
+    p.q_seq = qs.q_seq;
+    p.q_pos = qs.q_pos;
+    p.q_idx = q_idx;
+    p.w = w;
+    p.nq = qs.nq;
+    p.group = qs.group;
+    p.n_groups = qs.nq / qs.group;
+    p.h_idx = h_idx;
+    p.n_pad = ((qs.group * h_idx + 15) / 16) * 16;
+    p.max_n = max_n;
+    p.pool_blk = pool_blk;
+    p.pool_n = pool_n;
+    p.pool_blocks = pool_blocks;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    p.q8img = wsb;
+    wsb += align_up((size_t)p.n_groups * p.n_pad * c.d_idx, 256);
+    p.ws = reinterpret_cast<float *>(wsb);
+    wsb += align_up((size_t)qs.nq * h_idx * 4, 256);
+    p.nt = reinterpret_cast<int32_t *>(wsb);
+    wsb += align_up((size_t)qs.nq * 4, 256);
+    p.gtiles = reinterpret_cast<int32_t *>(wsb);
+    p.scores = scores;
+    p.ld = ld;
+    p.blockmax = blockmax;
+    p.ld_bm = ld_bm;
+    p.n_valid = n_valid;
+    p.counters = counters;
+
+    CUtensorMap tmap;
+    cudaError_t e = make_tmap_rows_u8(&tmap, c.kidx, c.cap, c.d_idx,
+                                      pool_blk ? 8 : kTile, c.d_idx == 128 ? 128 : 64);
+    if (e != cudaSuccess) return e;
+
+    index_prep_kernel<<<p.n_groups, 256, 0, st>>>(p);
+    note_launch();
+
+    const int stages = (p.n_pad <= 64) ? 8 : 6;
+    const int nacc = (p.n_pad <= 64) ? 4 : 2;
+    const size_t smem = index_smem_bytes(c.d_idx, p.n_pad, stages, nacc);
+    const int grid = device_sm_count();
+    if (c.d_idx == 128) {
+        auto k = index_main_kernel<128>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kIdxThreads, smem, st>>>(tmap, p, stages, nacc);
+    } else {
+        auto k = index_main_kernel<64>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kIdxThreads, smem, st>>>(tmap, p, stages, nacc);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace csa2

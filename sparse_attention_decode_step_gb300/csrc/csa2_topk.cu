@@ -1,0 +1,391 @@
+// csa2_topk.cu -- per-query top-k by radix select, and the candidate pool.
+//
+// Top-k: the k largest scores, ties to the lower position, listed ascending
+// (the tie rule is this library's reading; the pages only say "top-k").
+// Scores become order-preserving uint32 keys (-0 == +0).  Three histogram
+// rounds (11 + 11 + 10 bits) find the exact k-th key T and how many keys equal
+// to T are taken; a final ordered compaction writes every key > T and the
+// first (lowest-position) keys == T.  Work is split into 4096-candidate chunks
+// so a 1M-candidate query spreads over 256 CTAs; histograms are merged with
+// global atomics (no CTA ever waits on another).
+//
+// Pool ([Notes] section 3): the same selection over the block maxima of a Full
+// layer (k = 2,048 blocks), then the count of visible positions they hold.
+#include "csa2_device.cuh"
+#include "csa2_internal.h"
+
+namespace csa2 {
+
+constexpr int kChunk = 4096;
+constexpr int kTkThreads = 256;
+constexpr int kPerThread = kChunk / kTkThreads;   // 16
+constexpr int kBins = 2048;
+
+struct TopkState {
+    uint32_t prefix;   // key bits fixed so far
+    int32_t k_rem;     // elements still to take among those matching prefix
+    int32_t n;         // candidates of this query
+    int32_t all;       // n <= k: every candidate is taken
+};
+
+struct TopkParams {
+    const float *scores;
+    int64_t ld;
+    const int32_t *n_valid;
+    int n_div8;                 // candidates = ceil(n_valid / 8) (block maxima)
+    const int32_t *pool_blk;    // candidate -> position map, or null
+    int pool_blocks;
+    int nq, k, n_chunks;
+    int32_t *idx_out;
+    int64_t ld_idx;
+    int32_t *cnt_out;
+    // workspace
+    uint32_t *hist;             // [3][nq][kBins]
+    TopkState *state;           // [nq]
+    uint32_t *ccount;           // [nq][n_chunks][2]  (gt, eq)
+    uint32_t *coff;             // [nq][n_chunks][2]  (out offset, eq before)
+};
+
+__device__ __forceinline__ int round_shift(int r) { return r == 0 ? 21 : (r == 1 ? 10 : 0); }
+__device__ __forceinline__ uint32_t round_bins(int r) { return r == 2 ? 1024u : 2048u; }
+
+__global__ void topk_init_kernel(TopkParams p)
+{
+    const int q = blockIdx.x;
+    for (int i = threadIdx.x; i < 3 * kBins; i += blockDim.x) {
+        const int r = i / kBins, b = i % kBins;
+        p.hist[((int64_t)r * p.nq + q) * kBins + b] = 0u;
+    }
+    if (threadIdx.x == 0) {
+        int n = p.n_valid[q];
+        if (p.n_div8) n = (n + 7) / 8;
+        if (n < 0) n = 0;
+        TopkState s;
+        s.prefix = 0u;
+        s.n = n;
+        s.all = (n <= p.k) ? 1 : 0;
+        s.k_rem = s.all ? n : p.k;
+        p.state[q] = s;
+        p.cnt_out[q] = s.all ? n : p.k;
+    }
+}
+
+__global__ void __launch_bounds__(kTkThreads) topk_hist_kernel(TopkParams p, int r)
+{
+    const int q = blockIdx.y, c = blockIdx.x;
+    const TopkState st = p.state[q];
+    if (st.all) return;
+    const int64_t i0 = (int64_t)c * kChunk;
+    if (i0 >= st.n) return;
+    __shared__ uint32_t h[kBins];
+    for (int i = threadIdx.x; i < kBins; i += kTkThreads) h[i] = 0u;
+    __syncthreads();
+    const float *row = p.scores + (int64_t)q * p.ld;
+    const int sh = round_shift(r);
+    const uint32_t mask = round_bins(r) - 1u;
+    for (int e = 0; e < kPerThread; ++e) {
+        const int64_t i = i0 + e * kTkThreads + threadIdx.x;
+        if (i < st.n) {
+            const uint32_t key = score_key(row[i]);
+            bool match = (r == 0) || ((key >> (sh + (r == 1 ? 11 : 10))) == st.prefix);
+            if (match) atomicAdd(&h[(key >> sh) & mask], 1u);
+        }
+    }
+    __syncthreads();
+    uint32_t *gh = p.hist + ((int64_t)r * p.nq + q) * kBins;
+    for (int i = threadIdx.x; i < (int)round_bins(r); i += kTkThreads)
+        if (h[i]) atomicAdd(gh + i, h[i]);
+}
+
+// Block-wide exclusive scan of one value per thread (kTkThreads threads).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *s_warp, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = (lane < kTkThreads / 32) ? s_warp[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kTkThreads / 32) s_warp[lane] = w;   // inclusive warp totals
+    }
+    __syncthreads();
+    const uint32_t before = (warp > 0) ? s_warp[warp - 1] : 0u;
+    if (total) *total = s_warp[kTkThreads / 32 - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+// Picks the digit of round r: bins are scanned from the top; the digit d has
+// count(> d) < k_rem <= count(>= d).
+__global__ void __launch_bounds__(kTkThreads) topk_scan_kernel(TopkParams p, int r)
+{
+    const int q = blockIdx.x;
+    TopkState st = p.state[q];
+    if (st.all) return;
+    const uint32_t nb = round_bins(r);
+    const uint32_t per = nb / kTkThreads;      // 8 or 4 bins per thread, descending digits
+    const uint32_t *gh = p.hist + ((int64_t)r * p.nq + q) * kBins;
+    uint32_t cnt[8];
+    uint32_t mine = 0;
+    for (uint32_t i = 0; i < per; ++i) {
+        const uint32_t d = nb - 1u - (threadIdx.x * per + i);
+        cnt[i] = gh[d];
+        mine += cnt[i];
+    }
+    __shared__ uint32_t s_warp[kTkThreads / 32];
+    __shared__ uint32_t s_digit, s_above;
+    if (threadIdx.x == 0) { s_digit = 0; s_above = 0; }
+    __syncthreads();
+    uint32_t before = block_excl_scan(mine, s_warp, nullptr);
+    const uint32_t need = (uint32_t)st.k_rem;
+    if (before < need && need <= before + mine) {
+        uint32_t acc = before;
+        for (uint32_t i = 0; i < per; ++i) {
+            if (need <= acc + cnt[i]) {
+                s_digit = nb - 1u - (threadIdx.x * per + i);
+                s_above = acc;
+                break;
+            }
+            acc += cnt[i];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int bits = (r == 2) ? 10 : 11;
+        st.prefix = (st.prefix << bits) | s_digit;
+        st.k_rem -= (int32_t)s_above;
+        p.state[q] = st;
+    }
+}
+
+__device__ __forceinline__ void load16(const float *row, int64_t i0, int64_t n, uint32_t (&key)[16],
+                                       bool (&ok)[16])
+{
+    // 16 consecutive candidates i0..i0+15 of this thread
+    if (i0 + 16 <= n) {
+        const float4 *v4 = reinterpret_cast<const float4 *>(row + i0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float4 v = v4[j];
+            key[4 * j] = score_key(v.x);
+            key[4 * j + 1] = score_key(v.y);
+            key[4 * j + 2] = score_key(v.z);
+            key[4 * j + 3] = score_key(v.w);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ok[j] = true;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            ok[j] = (i0 + j) < n;
+            key[j] = ok[j] ? score_key(row[i0 + j]) : 0u;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTkThreads) topk_count_kernel(TopkParams p)
+{
+    const int q = blockIdx.y, c = blockIdx.x;
+    const TopkState st = p.state[q];
+    const int64_t i0 = (int64_t)c * kChunk + threadIdx.x * kPerThread;
+    uint32_t gt = 0, eq = 0;
+    if (!st.all) {
+        uint32_t key[16];
+        bool ok[16];
+        load16(p.scores + (int64_t)q * p.ld, i0, st.n, key, ok);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            gt += (ok[j] && key[j] > st.prefix);
+            eq += (ok[j] && key[j] == st.prefix);
+        }
+    } else {
+        gt = (uint32_t)max((int64_t)0, min((int64_t)kPerThread, (int64_t)st.n - i0));
+    }
+    __shared__ uint32_t s_warp[kTkThreads / 32];
+    uint32_t tgt, teq;
+    block_excl_scan(gt, s_warp, &tgt);
+    block_excl_scan(eq, s_warp, &teq);
+    if (threadIdx.x == 0) {
+        uint32_t *cc = p.ccount + ((int64_t)q * p.n_chunks + c) * 2;
+        cc[0] = tgt;
+        cc[1] = teq;
+    }
+}
+
+__global__ void __launch_bounds__(kTkThreads) topk_offsets_kernel(TopkParams p)
+{
+    const int q = blockIdx.x;
+    const TopkState st = p.state[q];
+    const int32_t k_eq = st.all ? 0 : st.k_rem;
+    __shared__ uint32_t s_warp[kTkThreads / 32];
+    __shared__ uint32_t s_carry_out, s_carry_eq;
+    if (threadIdx.x == 0) { s_carry_out = 0; s_carry_eq = 0; }
+    __syncthreads();
+    for (int c0 = 0; c0 < p.n_chunks; c0 += kTkThreads) {
+        const int c = c0 + threadIdx.x;
+        uint32_t gt = 0, eq = 0;
+        if (c < p.n_chunks) {
+            const uint32_t *cc = p.ccount + ((int64_t)q * p.n_chunks + c) * 2;
+            gt = cc[0];
+            eq = cc[1];
+        }
+        uint32_t eq_tot;
+        const uint32_t eq_before = s_carry_eq + block_excl_scan(eq, s_warp, &eq_tot);
+        int64_t take = (int64_t)k_eq - (int64_t)eq_before;
+        take = take < 0 ? 0 : (take > eq ? eq : take);
+        uint32_t out_tot;
+        const uint32_t out_before = s_carry_out + block_excl_scan(gt + (uint32_t)take, s_warp, &out_tot);
+        if (c < p.n_chunks) {
+            uint32_t *co = p.coff + ((int64_t)q * p.n_chunks + c) * 2;
+            co[0] = out_before;
+            co[1] = eq_before;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) { s_carry_out += out_tot; s_carry_eq += eq_tot; }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kTkThreads) topk_write_kernel(TopkParams p)
+{
+    const int q = blockIdx.y, c = blockIdx.x;
+    const TopkState st = p.state[q];
+    const int64_t i0 = (int64_t)c * kChunk + threadIdx.x * kPerThread;
+    if ((int64_t)c * kChunk >= st.n) return;
+    const uint32_t *co = p.coff + ((int64_t)q * p.n_chunks + c) * 2;
+    const uint32_t out0 = co[0], eqb = co[1];
+    uint32_t key[16];
+    bool ok[16];
+    uint32_t sel_mask = 0, eq_mask = 0;
+    if (st.all) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) if (i0 + j < st.n) sel_mask |= 1u << j;
+    } else {
+        load16(p.scores + (int64_t)q * p.ld, i0, st.n, key, ok);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (ok[j] && key[j] > st.prefix) sel_mask |= 1u << j;
+            if (ok[j] && key[j] == st.prefix) eq_mask |= 1u << j;
+        }
+    }
+    __shared__ uint32_t s_warp[kTkThreads / 32];
+    const uint32_t eq_rank0 = eqb + block_excl_scan(__popc(eq_mask), s_warp, nullptr);
+    uint32_t r = eq_rank0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (eq_mask & (1u << j)) {
+            if ((int64_t)r < (int64_t)st.k_rem) sel_mask |= 1u << j;
+            ++r;
+        }
+    }
+    uint32_t slot = out0 + block_excl_scan(__popc(sel_mask), s_warp, nullptr);
+    int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
+    const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (sel_mask & (1u << j)) {
+            const int64_t i = i0 + j;
+            const int32_t pos = pb ? 8 * pb[i >> 3] + (int32_t)(i & 7) : (int32_t)i;
+            if (slot < (uint32_t)p.k) out[slot] = pos;   // exactly min(k, n) slots exist
+            ++slot;
+        }
+    }
+}
+
+// Pool size: 8 per chosen block, minus the invisible tail of the newest block
+// when it is partial and was chosen.
+__global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
+                                  const int32_t *cnt, int32_t *pool_n, int nq)
+{
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= nq) return;
+    const int n = n_valid[q];
+    const int c = cnt[q];
+    int pn = 8 * c;
+    if (c > 0) {
+        const int last = pool_blk[(int64_t)q * pool_blocks + c - 1];
+        const int end = 8 * last + 8;
+        if (end > n) pn -= end - n;
+    }
+    pool_n[q] = pn;
+}
+
+// ---------------------------------------------------------------- host side
+size_t topk_workspace_bytes(int nq, int64_t max_n)
+{
+    const int64_t n_chunks = (max_n + kChunk - 1) / kChunk;
+    size_t s = align_up((size_t)3 * nq * kBins * 4, 256);
+    s += align_up((size_t)nq * sizeof(TopkState), 256);
+    s += align_up((size_t)nq * n_chunks * 8, 256) * 2;
+    return s;
+}
+
+cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid, int n_div8,
+                        const int32_t *pool_blk, int pool_blocks, int nq, int64_t max_n, int k,
+                        int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out, void *ws,
+                        cudaStream_t st)
+{
+    TopkParams p{};
+    p.scores = scores;
+    p.ld = ld;
+    p.n_valid = n_valid;
+    p.n_div8 = n_div8;
+    p.pool_blk = pool_blk;
+    p.pool_blocks = pool_blocks;
+    p.nq = nq;
+    p.k = k;
+    p.n_chunks = (int)((max_n + kChunk - 1) / kChunk);
+    if (p.n_chunks < 1) p.n_chunks = 1;
+    p.idx_out = idx_out;
+    p.ld_idx = ld_idx;
+    p.cnt_out = cnt_out;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    p.hist = reinterpret_cast<uint32_t *>(w);
+    w += align_up((size_t)3 * nq * kBins * 4, 256);
+    p.state = reinterpret_cast<TopkState *>(w);
+    w += align_up((size_t)nq * sizeof(TopkState), 256);
+    p.ccount = reinterpret_cast<uint32_t *>(w);
+    w += align_up((size_t)nq * p.n_chunks * 8, 256);
+    p.coff = reinterpret_cast<uint32_t *>(w);
+
+    const dim3 grid2(p.n_chunks, nq);
+    topk_init_kernel<<<nq, 256, 0, st>>>(p);
+    note_launch();
+    for (int r = 0; r < 3; ++r) {
+        topk_hist_kernel<<<grid2, kTkThreads, 0, st>>>(p, r);
+        topk_scan_kernel<<<nq, kTkThreads, 0, st>>>(p, r);
+        note_launch(2);
+    }
+    topk_count_kernel<<<grid2, kTkThreads, 0, st>>>(p);
+    topk_offsets_kernel<<<nq, kTkThreads, 0, st>>>(p);
+    topk_write_kernel<<<grid2, kTkThreads, 0, st>>>(p);
+    note_launch(3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_valid, int nq,
+                        int64_t max_n, int pool_blocks, int32_t *pool_blk, int32_t *pool_n,
+                        void *ws, cudaStream_t st)
+{
+    // the counts of chosen blocks go to pool_n first, then become positions
+    const int64_t max_blocks = (max_n + 7) / 8;
+    cudaError_t e = launch_topk(blockmax, ld_bm, n_valid, 1, nullptr, 0, nq, max_blocks,
+                                pool_blocks, pool_blk, pool_blocks, pool_n, ws, st);
+    if (e != cudaSuccess) return e;
+    pool_count_kernel<<<(nq + 127) / 128, 128, 0, st>>>(n_valid, pool_blk, pool_blocks, pool_n,
+                                                         pool_n, nq);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,357 @@
+"""Parity of each CUDA entry point with the float64 oracle, at sizes the oracle
+finishes in seconds that still span several tiles and a ragged tail.
+
+Bars: FP4 codes/scales and FP8 keys bit-exact; top-k indices and pools
+bit-exact on identical score arrays and end to end in exact-integer mode;
+scores and attention outputs within 2e-3 of the row's max |oracle| value."""
+import numpy as np
+import pytest
+import torch
+
+import csa2_inputs as ci
+import oracle as O
+import sparse_attention_decode_step_gb300 as csa
+from helpers import (TOL, bits16, build_gpu_cache, need_gpu, oracle_rows, oracle_seq_cache,
+                     rel_rows)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ================================================================ append
+@pytest.mark.parametrize("d_idx", [128, 64])
+def test_append_m1_bit_exact(d_idx):
+    wl = ci.Workload("t", 3, [1000, 333, 7], 0, 1, d_idx=d_idx, seed=11)
+    cnt = csa.new_counters()
+    cache = build_gpu_cache(wl, DEV, counters=cnt)
+    torch.cuda.synchronize()
+    assert _np(cache.seq_len).tolist() == [1000, 333, 7]
+    assert _np(cnt).tolist() == [0, 0, 0, 0]
+    for b, n in enumerate([1000, 333, 7]):
+        codes, scales, kidx, ksc, _ = oracle_rows(wl, b, 0, n)
+        r0 = cache.base_host[b]
+        assert np.array_equal(_np(cache.codes[r0:r0 + n]), codes)
+        assert np.array_equal(_np(cache.scales[r0:r0 + n]), scales)
+        assert np.array_equal(_np(cache.kidx[r0:r0 + n]), kidx)
+        assert np.array_equal(_np(cache.kscale[r0:r0 + n]), ksc)
+
+
+def test_append_batched_call_and_growth():
+    # one call appends to every sequence; a second call continues after it
+    wl = ci.Workload("t", 2, [0, 0], 0, 1, seed=12)
+    cache = csa.Cache([64, 64], 128, 1, DEV)
+    C = torch.stack([ci.latent_rows(wl, b, 0, 24, DEV)[0] for b in range(2)])
+    key = torch.stack([ci.key_rows(wl, b, 0, 24, DEV) for b in range(2)])
+    csa.quantize_append(cache, C[:, :10].contiguous(), None, key[:, :10].contiguous())
+    csa.quantize_append(cache, C[:, 10:].contiguous(), None, key[:, 10:].contiguous())
+    torch.cuda.synchronize()
+    assert _np(cache.seq_len).tolist() == [24, 24]
+    for b in range(2):
+        codes, scales, kidx, ksc, _ = oracle_rows(wl, b, 0, 24)
+        r0 = cache.base_host[b]
+        assert np.array_equal(_np(cache.codes[r0:r0 + 24]), codes)
+        assert np.array_equal(_np(cache.kidx[r0:r0 + 24]), kidx)
+
+
+def test_append_m2_exact_inputs_bit_exact():
+    # equal Z -> weights exactly 1/2; latents on a 2^-10 grid -> the block mean is exact in fp32
+    B, n_tok = 2, 64
+    g = torch.Generator().manual_seed(3)
+    C = (torch.randint(-4096, 4097, (B, n_tok, 512), generator=g).float() / 1024.0)
+    Z = torch.randn(B, n_tok // 2, 1, 512, generator=g).expand(B, n_tok // 2, 2, 512).reshape(B, n_tok, 512)
+    key = torch.randn(B, n_tok // 2, 128, generator=g)
+    cache = csa.Cache([64, 64], 128, 2, DEV)
+    csa.quantize_append(cache, C.to(DEV), Z.contiguous().to(DEV), key.to(DEV))
+    torch.cuda.synchronize()
+    codes, scales, kidx, ksc, x, _ = O.append(C.numpy(), Z.contiguous().numpy(), key.numpy(), 2)
+    for b in range(B):
+        r0 = cache.base_host[b]
+        sl = slice(b * 32, b * 32 + 32)
+        assert np.array_equal(_np(cache.codes[r0:r0 + 32]), codes[sl])
+        assert np.array_equal(_np(cache.scales[r0:r0 + 32]), scales[sl])
+        assert np.array_equal(_np(cache.kidx[r0:r0 + 32]), kidx[sl])
+
+
+def test_append_m2_random_differs_only_at_rounding_boundaries():
+    wl = ci.Workload("t", 1, [4096], 0, 2, d_idx=64, seed=13)
+    cache = build_gpu_cache(wl, DEV)
+    torch.cuda.synchronize()
+    n = 2048
+    codes, scales, kidx, ksc, x = oracle_rows(wl, 0, 0, n)
+    gc, gs = _np(cache.codes[:n]), _np(cache.scales[:n])
+    assert np.array_equal(_np(cache.kidx[:n]), kidx)
+    ok_scale = gs == scales
+    for r, g in np.argwhere(~ok_scale):
+        # a different scale only where amax / 6 sits on an E4M3 value (fp32 vs fp64 edge)
+        amax = np.abs(x[r, 16 * g:16 * g + 16]).max()
+        edge = 6.0 * min(O.e4m3_value(int(gs[r, g])), O.e4m3_value(int(scales[r, g])))
+        assert abs(amax - edge) <= 1e-5 * amax, (r, g)
+    assert (~ok_scale).sum() <= 2
+    dg = O.fp4_decode_rows(gc, gs)
+    do = O.fp4_decode_rows(codes, scales)
+    same_scale = np.repeat(ok_scale, 16, axis=1)
+    diff = np.argwhere((dg != do) & same_scale)
+    assert len(diff) <= n * 512 * 1e-3
+    for r, c in diff:
+        # the fp64 value sits on the rounding midpoint the fp32 value fell across
+        mid = 0.5 * (dg[r, c] + do[r, c])
+        assert abs(x[r, c] - mid) <= 1e-5 * abs(mid), (r, c, x[r, c], dg[r, c], do[r, c])
+
+
+def test_append_saturation_and_capacity_counters():
+    cache = csa.Cache([16], 128, 1, DEV)
+    C = torch.zeros(1, 8, 512)
+    C[0, 0, :16] = 3000.0          # one saturated group
+    C[0, 3, 100] = -5000.0         # another
+    key = torch.ones(1, 8, 128)
+    cnt = csa.new_counters()
+    csa.quantize_append(cache, C.to(DEV), None, key.to(DEV), counters=cnt)
+    csa.quantize_append(cache, C.to(DEV), None, key.to(DEV), counters=cnt)
+    csa.quantize_append(cache, C.to(DEV), None, key.to(DEV), counters=cnt)   # 24 > 16: refused
+    torch.cuda.synchronize()
+    assert _np(cnt).tolist() == [4, 1, 0, 0]
+    assert int(cache.seq_len[0]) == 16
+    codes, scales, _k, _s, _x, nsat = O.append(C.numpy(), None, key.numpy(), 1)
+    assert nsat == 2
+    assert np.array_equal(_np(cache.codes[:8]), codes) and np.array_equal(_np(cache.scales[8:16]), scales)
+
+
+# ================================================================ indexer
+def _index_case(wl, lengths, positions, exact):
+    cache = build_gpu_cache(wl, DEV)
+    q_seq = [b for b, _ in positions]
+    q_pos = [t for _, t in positions]
+    qs = csa.Queries(q_seq, q_pos, 1, DEV)
+    qi, w, _qa = ci.query_inputs(wl, len(q_seq), "cpu")
+    max_n = max(lengths)
+    ld = (max_n + 3) // 4 * 4
+    scores = torch.full((len(q_seq), ld), float("nan"), device=DEV)
+    bm = torch.full((len(q_seq), (max_n + 7) // 8 + 4), float("nan"), device=DEV)
+    nv = torch.zeros(len(q_seq), dtype=torch.int32, device=DEV)
+    cnt = csa.new_counters()
+    csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), max_n, scores, blockmax=bm, n_valid=nv,
+                   counters=cnt)
+    torch.cuda.synchronize()
+    assert _np(cnt).tolist() == [0, 0, 0, 0]
+    gs, gb = _np(scores), _np(bm)
+    for i, (b, t) in enumerate(positions):
+        n = (t + 1) // wl.m
+        assert int(nv[i]) == n
+        oc = oracle_seq_cache(wl, b, n)
+        ref = O.scores_full(oc["kidx"], oc["kscale"], qi[i].numpy(), w[i].numpy(), 0, n)
+        refbm = O.blockmax(ref)
+        if exact:
+            assert np.array_equal(gs[i, :n].astype(np.float64), ref), i
+            assert np.array_equal(gb[i, :(n + 7) // 8].astype(np.float64), refbm), i
+        else:
+            assert rel_rows(gs[i, :n][None], ref[None])[0] <= TOL
+            assert rel_rows(gb[i, :(n + 7) // 8][None], refbm[None])[0] <= TOL
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_index_full_ragged_batch(exact):
+    lengths = [5000, 130, 1029]
+    wl = ci.Workload("t", 3, lengths, 0, 1, exact=exact, seed=21)
+    positions = [(0, 4999), (1, 129), (2, 1028), (0, 2047), (2, 7), (0, 0)]
+    _index_case(wl, lengths, positions, exact)
+
+
+def test_index_full_tiny_shape_m2():
+    # d_idx 64, 4 indexer heads, m = 2 (tiny workload shape)
+    wl = ci.Workload("t", 1, [4096], 0, 2, h_idx=4, d_idx=64, exact=True, seed=22)
+    _index_case(wl, [2048], [(0, 4095), (0, 4094), (0, 1001)], True)
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_index_full_grouped_prefill(exact):
+    # 64 causal queries of one sequence scored together (groups of 32, N = 256)
+    wl = ci.Workload("t", 1, [6000], 0, 2, exact=exact, seed=23)
+    cache = build_gpu_cache(wl, DEV)
+    nq = 64
+    q_pos = [5936 + i for i in range(nq)]
+    qs = csa.Queries([0] * nq, q_pos, 32, DEV)
+    qi, w, _ = ci.query_inputs(wl, nq, "cpu")
+    max_n = 3000
+    scores = torch.full((nq, max_n), float("nan"), device=DEV)
+    bm = torch.full((nq, max_n // 8), float("nan"), device=DEV)
+    csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), max_n, scores, blockmax=bm)
+    torch.cuda.synchronize()
+    oc = oracle_seq_cache(wl, 0, 3000)
+    gs, gb = _np(scores), _np(bm)
+    for i in range(nq):
+        n = (q_pos[i] + 1) // 2
+        ref = O.scores_full(oc["kidx"], oc["kscale"], qi[i].numpy(), w[i].numpy(), 0, n)
+        if exact:
+            assert np.array_equal(gs[i, :n].astype(np.float64), ref), i
+            assert np.array_equal(gb[i, :(n + 7) // 8].astype(np.float64), O.blockmax(ref)), i
+        else:
+            assert rel_rows(gs[i, :n][None], ref[None])[0] <= TOL
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_index_reindex_pool(exact):
+    n = 20000
+    wl = ci.Workload("t", 2, [n, 9000], 0, 1, exact=exact, seed=24)
+    cache = build_gpu_cache(wl, DEV)
+    rng = np.random.default_rng(5)
+    pool_blocks = 2048
+    blk0 = np.sort(rng.choice(n // 8, 2048, replace=False)).astype(np.int32)
+    blk1 = np.sort(rng.choice(9000 // 8, 700, replace=False)).astype(np.int32)
+    pool = np.zeros((2, pool_blocks), np.int32)
+    pool[0] = blk0
+    pool[1, :700] = blk1
+    pool_n = np.array([8 * 2048, 8 * 700 - 3], np.int32)     # ragged tail on query 1
+    qs = csa.Queries([0, 1], [n - 1, 8999], 1, DEV)
+    qi, w, _ = ci.query_inputs(wl, 2, "cpu")
+    scores = torch.full((2, 8 * pool_blocks), float("nan"), device=DEV)
+    nv = torch.zeros(2, dtype=torch.int32, device=DEV)
+    csa.index_reindex(cache, qs, qi.to(DEV), w.to(DEV), torch.from_numpy(pool).to(DEV),
+                      torch.from_numpy(pool_n).to(DEV), scores, n_valid=nv)
+    torch.cuda.synchronize()
+    gs = _np(scores)
+    for i, (nn, pn) in enumerate([(n, pool_n[0]), (9000, pool_n[1])]):
+        assert int(nv[i]) == pn
+        oc = oracle_seq_cache(wl, i, nn)
+        rows = np.array([8 * pool[i, p // 8] + p % 8 for p in range(pn)], np.int64)
+        ref = O.scores_at(oc["kidx"], oc["kscale"], qi[i].numpy(), w[i].numpy(), rows)
+        if exact:
+            assert np.array_equal(gs[i, :pn].astype(np.float64), ref)
+        else:
+            assert rel_rows(gs[i, :pn][None], ref[None])[0] <= TOL
+
+
+def test_index_counts_query_past_cache():
+    wl = ci.Workload("t", 1, [100], 0, 1, seed=25)
+    cache = build_gpu_cache(wl, DEV)
+    qs = csa.Queries([0, 0], [99, 150], 1, DEV)          # second query: position not cached
+    qi, w, _ = ci.query_inputs(wl, 2, "cpu")
+    scores = torch.zeros(2, 256, device=DEV)
+    nv = torch.zeros(2, dtype=torch.int32, device=DEV)
+    cnt = csa.new_counters()
+    csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), 256, scores, n_valid=nv, counters=cnt)
+    torch.cuda.synchronize()
+    assert int(cnt[csa.CNT_BAD_INPUT]) == 1 and _np(nv).tolist() == [100, 0]
+
+
+# ================================================================ top-k and pool
+def _topk_gpu(scores_np, nvalid, k, pool=None, ld=None):
+    nq, n = scores_np.shape
+    ld = ld or (n + 3) // 4 * 4
+    s = torch.zeros(nq, ld, dtype=torch.float32)
+    s[:, :n] = torch.from_numpy(scores_np)
+    idx = torch.full((nq, k), -1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(nq, dtype=torch.int32, device=DEV)
+    csa.topk(s.to(DEV), torch.tensor(nvalid, dtype=torch.int32, device=DEV), k, idx, cnt,
+             max_n=n, pool_blk=None if pool is None else torch.from_numpy(pool).to(DEV))
+    torch.cuda.synchronize()
+    return _np(idx), _np(cnt)
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (100, 7), (4096, 64), (4097, 4096), (70001, 2048),
+                                 (300, 2048), (16384, 2048)])
+def test_topk_bit_exact(n, k):
+    rng = np.random.default_rng(n + k)
+    s = rng.normal(size=(3, n)).astype(np.float32)
+    s[1] = np.round(s[1] * 4) / 4                       # heavy ties
+    s[2, ::7] = 0.0
+    s[2, 3::7] = -0.0                                   # -0 equals +0
+    nvalid = [n, max(1, n - 5), max(1, n // 3)]
+    idx, cnt = _topk_gpu(s, nvalid, k)
+    for i in range(3):
+        ref = O.topk(s[i, :nvalid[i]], k)
+        assert cnt[i] == len(ref)
+        assert np.array_equal(idx[i, :cnt[i]], ref), i
+
+
+def test_topk_with_pool_map():
+    rng = np.random.default_rng(1)
+    pool = np.sort(rng.choice(100000, 2048, replace=False)).astype(np.int32)[None].repeat(2, 0)
+    pn = [16384, 16381]
+    s = np.round(rng.normal(size=(2, 16384)) * 8).astype(np.float32) / 8
+    idx, cnt = _topk_gpu(s, pn, 2048, pool=pool)
+    for i in range(2):
+        pos = np.array([8 * pool[i, p // 8] + p % 8 for p in range(pn[i])], np.int32)
+        ref = O.topk(s[i, :pn[i]], 2048, pos)
+        assert np.array_equal(idx[i, :cnt[i]], ref)
+
+
+@pytest.mark.parametrize("n", [50, 16384, 16387, 200003])
+def test_pool_select_bit_exact(n):
+    rng = np.random.default_rng(n)
+    sc = rng.normal(size=n)
+    sc[-1] = 40.0                                        # newest (maybe partial) block wins
+    refbm = O.blockmax(sc)
+    nb = len(refbm)
+    bm = torch.zeros(1, (nb + 3) // 4 * 4, dtype=torch.float32)
+    bm[0, :nb] = torch.from_numpy(refbm.astype(np.float32))
+    blk = torch.full((1, 2048), -1, dtype=torch.int32, device=DEV)
+    pn = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa.pool_select(bm.to(DEV), torch.tensor([n], dtype=torch.int32, device=DEV), n, blk, pn)
+    torch.cuda.synchronize()
+    # the oracle sees the same fp32 block maxima (each repeated over its block)
+    ref_blk, ref_pn = O.pool(np.repeat(refbm.astype(np.float32), 8)[:n].astype(np.float64), 2048)
+    c = min(2048, nb)
+    assert np.array_equal(_np(blk)[0, :c], ref_blk) and int(pn[0]) == ref_pn
+
+
+# ================================================================ attention
+def _attn_case(H, n_ent, cnts, n_win, wcap, win_start=None, sm=1.0, seed=31, bad=False):
+    nq = len(cnts)
+    wl = ci.Workload("t", nq, [n_ent] * nq, 0, 1, heads=H, seed=seed)
+    cache = build_gpu_cache(wl, DEV)
+    rng = np.random.default_rng(seed)
+    k_max = max(max(cnts), 1)
+    idx = np.zeros((nq, k_max), np.int32)
+    for i, c in enumerate(cnts):
+        idx[i, :c] = np.sort(rng.choice(n_ent, c, replace=False))
+    if bad:
+        idx[0, 0] = n_ent + 5
+    _qi, _w, qa = ci.query_inputs(wl, nq, "cpu")
+    win = ci.window_rows(wl, nq, wcap, "cpu")
+    qs = csa.Queries(list(range(nq)), [n_ent - 1] * nq, 1, DEV)
+    out = torch.full((nq, H, 512), float("nan"), device=DEV)
+    lse = torch.full((nq, H), float("nan"), device=DEV)
+    cnt = csa.new_counters()
+    ws_t = None if win_start is None else torch.tensor(win_start, dtype=torch.int32, device=DEV)
+    csa.sparse_attn(cache, qs, torch.from_numpy(idx).to(DEV),
+                    torch.tensor(cnts, dtype=torch.int32, device=DEV), qa.to(DEV),
+                    win.to(DEV) if n_win else None, n_win, out, lse=lse, win_start=ws_t,
+                    sm_scale=sm, counters=cnt)
+    torch.cuda.synchronize()
+    go, gl = _np(out), _np(lse)
+    for i in range(nq):
+        codes, scales, _k, _s, _x = oracle_rows(wl, i, 0, n_ent)
+        sel = idx[i, :cnts[i]]
+        if bad and i == 0:
+            sel = sel[1:]
+        s = 0 if win_start is None else win_start[i]
+        rows = O.gather_rows(codes, scales, 0, sel, bits16(win[i]) if n_win else None, wcap,
+                             n_ent - 1, s, n_win)
+        ref, rlse = O.attention(bits16(qa[i]), rows, sm)
+        assert rel_rows(go[i], ref).max() <= TOL, i
+        assert np.abs(gl[i] - rlse).max() <= 1e-3 * max(1.0, np.abs(rlse).max())
+    return _np(cnt)
+
+
+@pytest.mark.parametrize("H", [64, 16])
+def test_attention_matches_oracle(H):
+    c = _attn_case(H, 3000, [2048, 5, 0, 1000], 128, 256)
+    assert c.tolist() == [0, 0, 0, 0]
+
+
+def test_attention_window_truncation_and_scale():
+    _attn_case(64, 600, [300, 17], 128, 128, win_start=[560, 0], sm=0.37, seed=32)
+
+
+def test_attention_counts_and_skips_bad_index():
+    c = _attn_case(32, 500, [40, 40], 16, 32, seed=33, bad=True)
+    assert c[csa.CNT_BAD_INPUT] == 1
