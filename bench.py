@@ -1,0 +1,434 @@
+"""Benchmark of the CSA2 decode step on GB300 (one JSON line on stdout).
+
+Workload (default): decoder Full-mode decode, 32 sequences x 65,536 cached
+tokens (m = 1), 8 indexer heads x 128 (FP8), 64 query heads, top-2048,
+128-token window.  One step = append of the new token of every sequence
+(FP4 latent + FP8 key) -> Full-mode indexer over the whole visible context ->
+top-k -> sparse attention over the 2,048 selected entries + the window.
+Metric: decode queries per second per layer (higher is better).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl csa2|reference]
+
+`value`: device time of K steps with every input already in HBM; each step is
+a CUDA-graph replay timed with CUDA events; L2 is flushed (a 512 MB write)
+between steps, outside the timed events.  `e2e`: the same steps through the
+public layer call with host (pinned) inputs copied in and the output copied
+back inside the timed region.  With N > 1 (torchrun) every rank runs its own
+replica of the workload (weak scaling, no collective on the data path) and
+the time is the max over ranks.  `--impl reference` times the float64 CPU
+oracle on the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import csa2_inputs as ci  # noqa: E402
+
+METRIC = "CSA2 decode queries/s/layer at 64K-1M ctx; HBM GB/s & FP8 util vs GB300 peak"
+UNIT = "queries/s/layer"
+L2_FLUSH_BYTES = 512 << 20
+# algorithmic bytes of the Full-mode indexer per visible entry: 128 B FP8 key +
+# 4 B key scale read, 4 B score written
+IDX_BYTES_PER_ENTRY = 128 + 4 + 4
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "index_main_decode_b32_ctx65536.md")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the indexer from the committed ncu summary."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    for line in open(PROFILE_SUMMARY):
+        if line.startswith("traffic_bytes_per_launch_scaled:"):
+            v = line.split(":", 1)[1].strip()
+            return None if v in ("", "null") else float(v)
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+def build_cache(csa, wl, dev, extra):
+    """Fills every sequence's cache through the library's append (m = 1 here)."""
+    caps = [(t + wl.new_tokens) // wl.m + extra for t in wl.ctx_tokens]
+    cache = csa.Cache(caps, wl.d_idx, wl.m, dev)
+    chunk = 65536
+    for b, T in enumerate(wl.ctx_tokens):
+        done = 0
+        while done < T:
+            n = min(chunk, T - done)
+            C, Z = ci.latent_rows(wl, b, done, n, dev)
+            key = ci.key_rows(wl, b, done // wl.m, n // wl.m, dev)
+            csa.quantize_append(cache, C[None].contiguous(),
+                                None if Z is None else Z[None].contiguous(), key[None].contiguous(),
+                                seq=b)
+            done += n
+    torch.cuda.synchronize()
+    return cache
+
+
+def step_inputs(wl, step, B, dev):
+    """Inputs of decode step `step`: the new token of every sequence, the
+    indexer and attention queries of the layer."""
+    T0 = wl.ctx_tokens[0]
+    C = torch.stack([ci.latent_rows(wl, b, T0 + step, 1, dev)[0] for b in range(B)])
+    key = torch.stack([ci.key_rows(wl, b, T0 + step, 1, dev) for b in range(B)])
+    qi, w, qa = ci.query_inputs(wl, B, dev, layer=1000 + step)
+    return dict(C=C.contiguous(), key=key.contiguous(), q_idx=qi.contiguous(), w=w.contiguous(),
+                q=qa.contiguous())
+
+
+def run_csa2(args, rank, world):
+    import sparse_attention_decode_step_gb300 as csa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = ci.config(2)
+    B = wl.batch
+    T0 = wl.ctx_tokens[0]
+    n_steps = args.warmup + args.steps
+    cache = build_cache(csa, wl, dev, extra=2 * n_steps + 16)   # value steps + e2e steps
+    wcap = 512
+    win = ci.window_rows(wl, B, wcap, dev)          # ring buffers; every needed position filled
+
+    # fixed staging buffers (the graph's inputs) and outputs
+    stage = step_inputs(wl, 0, B, dev)
+    inputs = [step_inputs(wl, s, B, dev) for s in range(n_steps)]
+    q_pos = torch.full((B,), T0, dtype=torch.int32, device=dev)
+    qs = csa.Queries(list(range(B)), [T0] * B, 1, dev)
+    max_n = T0 + n_steps + 1
+    ld = (max_n + 3) // 4 * 4
+    scores = torch.empty(B, ld, device=dev)
+    nv = torch.empty(B, dtype=torch.int32, device=dev)
+    idx = torch.empty(B, wl.k, dtype=torch.int32, device=dev)
+    cnt = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, wl.heads, 512, device=dev)
+    lse = torch.empty(B, wl.heads, device=dev)
+    counters = csa.new_counters(dev)
+    iws = csa.workspace(csa.index_workspace_size(B, 1, wl.h_idx, wl.d_idx), dev)
+    tws = csa.workspace(csa.topk_workspace_size(B, max_n), dev)
+    aws = csa.workspace(csa.attn_workspace_size(B, wl.heads, wl.k, wl.n_win), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    outer = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def phases():
+        ev[0].record()
+        csa.quantize_append(cache, stage["C"], None, stage["key"], counters=counters)
+        ev[1].record()
+        csa.index_full(cache, qs, stage["q_idx"], stage["w"], max_n, scores, n_valid=nv, ws=iws,
+                       counters=counters)
+        ev[2].record()
+        csa.topk(scores, nv, wl.k, idx, cnt, max_n=max_n, ws=tws)
+        ev[3].record()
+        csa.sparse_attn(cache, qs, idx, cnt, stage["q"], win, wl.n_win, out, lse=lse,
+                        ws=aws, counters=counters)
+        ev[4].record()
+
+    def load_step(s):
+        for k_ in stage:
+            stage[k_].copy_(inputs[s][k_])
+        qs.q_pos.fill_(T0 + s)
+
+    # capture one step as a CUDA graph (queries advance one position per step)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    l0 = csa.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    # rows appended during capture must not count: the graph is captured, not run
+    with torch.cuda.graph(graph, stream=side):
+        phases()
+    launches_per_step = csa.launch_count() - l0
+
+    times, ph, ph_ok = [], np.zeros(4), True
+    clocks = Clocks(torch.cuda.current_device())
+    torch.cuda.synchronize()
+    for s in range(n_steps):
+        load_step(s)
+        flush.fill_(s & 0xFF)                      # evict L2 between steps (not timed)
+        if s == args.warmup:
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            clocks.__enter__()
+        outer[0].record()
+        graph.replay()
+        outer[1].record()
+        if s >= args.warmup:
+            torch.cuda.synchronize()
+            times.append(outer[0].elapsed_time(outer[1]) / 1e3)
+            try:
+                ph += [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(4)]
+            except RuntimeError:
+                ph_ok = False
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.__exit__(None, None, None)
+    total = sum(times)
+    if world > 1:
+        t = torch.tensor([total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
+    ph /= args.steps
+    if not ph_ok:
+        ph = phase_times_eager(phases, ev, load_step, n_steps - 1)
+    ms = total / args.steps * 1e3
+
+    # ---- end to end: pinned host inputs in, output back, through the layer call
+    e2e = run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world)
+
+    # ---- roofline of the dominant kernel (Full-mode indexer)
+    hbm, bf16, src = peaks()
+    entries = sum(T0 + args.warmup + s + 1 for s in range(args.steps)) / args.steps * B
+    idx_bytes = entries * IDX_BYTES_PER_ENTRY
+    achieved = idx_bytes / ph[1] / 1e9
+    traffic = profiled_traffic()
+    roof = {"kernel": "index_main_kernel (+ index_prep_kernel)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_source": src,
+            "traffic": None if traffic is None else round(traffic * entries / (B * 65536)),
+            "algorithmic_bytes_per_launch": round(idx_bytes)}
+    attn_bytes = B * (wl.k * 288 + wl.n_win * 1024 + wl.heads * 512 * 2 + wl.heads * 512 * 4 +
+                      wl.k * 4)
+    attn_flops = B * 4 * wl.heads * 512 * (wl.k + wl.n_win)
+    res = {
+        "metric": METRIC, "value": round(world * B * args.steps / total, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (indexer MMA), fp4/bf16 -> fp32 (attention)",
+        "data": "synthetic (seeded counter-hash generator; N(0,1) latents scaled to norm sqrt(512))",
+        "config": {"workload": wl.name, "batch": B, "ctx_tokens": T0 + 1, "m": wl.m,
+                   "indexer_heads": wl.h_idx, "d_idx": wl.d_idx, "heads": wl.heads, "k": wl.k,
+                   "n_win": wl.n_win, "layers": 1, "l2": "flushed between steps (512 MB write)",
+                   "graph": "one CUDA graph replay per step", "parallelism": f"replicas x{world}"},
+        "phases_us": {"append": round(ph[0] * 1e6, 2), "index_full": round(ph[1] * 1e6, 2),
+                      "topk": round(ph[2] * 1e6, 2), "sparse_attn": round(ph[3] * 1e6, 2)},
+        "attn_roofline": {"bytes": attn_bytes, "flops": attn_flops,
+                          "hbm_frac": round(attn_bytes / ph[3] / 1e9 / hbm, 4),
+                          "bf16_frac": round(attn_flops / ph[3] / 1e12 / bf16, 4)},
+        "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        res["cpu_baseline"] = cpu_baseline(wl, cache, win, inputs[args.warmup], T0 + args.warmup)
+    return res
+
+
+def phase_times_eager(phases, ev, load_step, s):
+    """Phase durations from one eager (non-graph) run, when graph-captured
+    events cannot be timed."""
+    load_step(s)
+    torch.cuda.synchronize()
+    phases()
+    torch.cuda.synchronize()
+    return np.array([ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(4)])
+
+
+def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
+    """Pinned host inputs -> device -> layer call -> output back to the host."""
+    host = [{k_: v.cpu().pin_memory() for k_, v in step_inputs(wl, s, B, "cpu").items()}
+            for s in range(n_steps)]
+    dstage = {k_: torch.empty_like(v, device=dev) for k_, v in host[0].items()}
+    qs = csa.Queries(list(range(B)), [T0] * B, 1, dev)
+    idx = torch.empty(B, wl.k, dtype=torch.int32, device=dev)
+    cnt = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, wl.heads, 512, device=dev)
+    out_h = torch.empty(B, wl.heads, 512).pin_memory()
+    max_n = T0 + 2 * n_steps + 2
+    layer = csa.Layer(csa.FULL, cache, qs, k=wl.k, q=dstage["q"], win=win, n_win=wl.n_win,
+                      out=out, idx=idx, cnt=cnt, q_idx=dstage["q_idx"], w=dstage["w"], max_n=max_n)
+    base_len = cache.seq_len.clone()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for s in range(n_steps):
+        qs.q_pos.copy_(base_len + s)      # the new token's position (after earlier appends)
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        e0.record()
+        for k_ in dstage:
+            dstage[k_].copy_(host[s][k_], non_blocking=True)
+        csa.quantize_append(cache, dstage["C"], None, dstage["key"])
+        layer()
+        out_h.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    total = sum(times)
+    if world > 1:
+        t = torch.tensor([total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    return {"value": round(world * B * args.steps / total, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 4,
+            "ms_per_step": round(total / args.steps * 1e3, 4)}
+
+
+def cpu_baseline(wl, cache, win, inp, t):
+    """The float64 oracle on a bounded sample: one step's 32 queries, each over
+    its full 65,536-entry context (host cores, OpenMP over queries)."""
+    import oracle as O
+    B = wl.batch
+    n = t + 1
+    rows = []
+    codes = cache.codes.cpu().numpy()
+    scales = cache.scales.cpu().numpy()
+    kidx = cache.kidx.cpu().numpy()
+    ksc = cache.kscale.cpu().numpy()
+    base = np.array(cache.base_host[:B], np.int64)
+    O.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    O.layer(O.FULL, codes=codes, scales=scales, kidx=kidx, kscale=ksc, seq_base=base, m=1,
+            q_seq=list(range(B)), q_pos=[t] * B, k=wl.k, H=wl.heads,
+            q_attn=inp["q"][:B].cpu().numpy().view(np.uint16),
+            win=win[:B].cpu().numpy().view(np.uint16), wcap=win.shape[1], n_win=wl.n_win,
+            sm_scale=1.0, q_idx=inp["q_idx"][:B].cpu().numpy(), w=inp["w"][:B].cpu().numpy())
+    dt = time.perf_counter() - t0
+    return {"value": round(B / dt, 3), "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+            "sample": f"{B} queries x {n} entries (one Full layer: scoring, top-{wl.k}, attention), "
+                      f"{dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle, timed on the host cores, on the same workload."""
+    if rank != 0:
+        return None
+    import oracle as O
+    wl = ci.config(2)
+    B_s = 4   # queries per step of the CPU sample
+    T0 = wl.ctx_tokens[0]
+    n = T0 + 1
+    # the sample's caches: oracle-encoded entries of B_s sequences
+    caches = []
+    for b in range(B_s):
+        C, _ = ci.latent_rows(wl, b, 0, n, "cpu")
+        key = ci.key_rows(wl, b, 0, n, "cpu")
+        codes, scales, kidx, ksc, _x, _ = O.append(C.numpy()[None], None, key.numpy()[None], 1)
+        caches.append((codes, scales, kidx, ksc))
+    codes = np.concatenate([c[0] for c in caches])
+    scales = np.concatenate([c[1] for c in caches])
+    kidx = np.concatenate([c[2] for c in caches])
+    ksc = np.concatenate([c[3] for c in caches])
+    base = np.arange(B_s, dtype=np.int64) * n
+    win = ci.window_rows(wl, B_s, 512, "cpu").numpy().view(np.uint16)
+    O.set_threads(os.cpu_count() or 1)
+    times = []
+    for s in range(args.warmup + args.steps):
+        qi, w, qa = ci.query_inputs(wl, wl.batch, "cpu", layer=1000 + s)
+        t0 = time.perf_counter()
+        O.layer(O.FULL, codes=codes, scales=scales, kidx=kidx, kscale=ksc, seq_base=base, m=1,
+                q_seq=list(range(B_s)), q_pos=[T0] * B_s, k=wl.k, H=wl.heads,
+                q_attn=qa[:B_s].numpy().view(np.uint16), win=win, wcap=512, n_win=wl.n_win,
+                sm_scale=1.0, q_idx=qi[:B_s].numpy(), w=w[:B_s].numpy())
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    v = round(B_s * args.steps / total, 3)
+    return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "batch": wl.batch, "ctx_tokens": n, "m": 1,
+                       "k": wl.k, "heads": wl.heads, "sample_queries_per_step": B_s},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+                             "sample": f"{B_s} of {wl.batch} queries per step, full 65,536-entry "
+                                       f"contexts, {args.steps} steps"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_csa2(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

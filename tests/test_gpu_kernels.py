@@ -135,7 +135,7 @@ def _index_case(wl, lengths, positions, exact):
     max_n = max(lengths)
     ld = (max_n + 3) // 4 * 4
     scores = torch.full((len(q_seq), ld), float("nan"), device=DEV)
-    bm = torch.full((len(q_seq), (max_n + 7) // 8 + 4), float("nan"), device=DEV)
+    bm = torch.full((len(q_seq), ((max_n + 7) // 8 + 3) // 4 * 4), float("nan"), device=DEV)
     nv = torch.zeros(len(q_seq), dtype=torch.int32, device=DEV)
     cnt = csa.new_counters()
     csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), max_n, scores, blockmax=bm, n_valid=nv,
@@ -182,7 +182,7 @@ def test_index_full_grouped_prefill(exact):
     qi, w, _ = ci.query_inputs(wl, nq, "cpu")
     max_n = 3000
     scores = torch.full((nq, max_n), float("nan"), device=DEV)
-    bm = torch.full((nq, max_n // 8), float("nan"), device=DEV)
+    bm = torch.full((nq, (max_n // 8 + 3) // 4 * 4), float("nan"), device=DEV)
     csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), max_n, scores, blockmax=bm)
     torch.cuda.synchronize()
     oc = oracle_seq_cache(wl, 0, 3000)
