@@ -80,7 +80,7 @@ class Clocks:
                  "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -206,7 +206,8 @@ def run_csa2(args, rank, world):
     launches_per_step = csa.launch_count() - l0
 
     times, ph, ph_ok = [], np.zeros(4), True
-    clocks = Clocks(torch.cuda.current_device())
+    # clocks are sampled from the start of the warm-up to the end of the timed steps
+    clocks = Clocks(torch.cuda.current_device()).__enter__()
     torch.cuda.synchronize()
     for s in range(n_steps):
         load_step(s)
@@ -216,7 +217,6 @@ def run_csa2(args, rank, world):
             if world > 1:
                 torch.distributed.barrier()
             torch.cuda.synchronize()
-            clocks.__enter__()
         outer[0].record()
         graph.replay()
         outer[1].record()
@@ -408,7 +408,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
     args = ap.parse_args()

@@ -64,21 +64,21 @@ cudaError_t make_tmap_rows_u8(CUtensorMap *map, const void *base, int64_t rows, 
 }
 
 // ---------------------------------------------------------------- attention plan
+// Rows of a query are processed in 128-row tiles; a query's tiles are split
+// over CTAs so that the grid fills the SMs in one wave (one CTA per SM: the
+// kernel uses ~210 KB of shared memory and all 512 TMEM columns).
 void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_split)
 {
     (void)H;
-    const int rows = k_max + n_win;
+    const int rows = k_max + n_win > 0 ? k_max + n_win : 1;
+    const int tiles = (rows + 127) / 128;
     const int sms = device_sm_count();
-    int s = (2 * sms + nq - 1) / (nq > 0 ? nq : 1);
-    const int smax = (rows + 63) / 64;
-    if (s > smax) s = smax;
+    int s = sms / (nq > 0 ? nq : 1);
+    if (s > tiles) s = tiles;
     if (s < 1) s = 1;
-    int rps = (rows + s - 1) / s;
-    rps = (rps + 31) / 32 * 32;
-    if (rps < 32) rps = 32;
-    *splits = (rows + rps - 1) / rps;
-    if (*splits < 1) *splits = 1;
-    *rows_per_split = rps;
+    const int tps = (tiles + s - 1) / s;
+    *rows_per_split = tps * 128;
+    *splits = (tiles + tps - 1) / tps;
 }
 
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win)
@@ -324,7 +324,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
     w += align_up((size_t)p.nq * p.splits * H * CSA2_D * 4, 256);
     p.part_ml = reinterpret_cast<float *>(w);
     p.counters = counters;
-    return cuda_status(launch_attn_simt(p, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_attn_tc(p, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- layer driver

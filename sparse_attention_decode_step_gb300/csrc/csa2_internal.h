@@ -75,5 +75,7 @@ struct AttnParams {
 void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_split);
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win);
 cudaError_t launch_attn_simt(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
+__global__ void attn_combine_kernel(AttnParams p);
 
 }  // namespace csa2
