@@ -114,6 +114,20 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def job_time(local_seconds, world, device):
+    """The job's time: the slowest rank's time (every rank ran its own replica)."""
+    if world <= 1:
+        return local_seconds
+    t = torch.tensor([local_seconds], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(queries_per_rank, world, seconds):
+    """Whole-job throughput: the queries of every rank over the job's time."""
+    return world * queries_per_rank / seconds
+
+
 # ------------------------------------------------------------------ workload
 def build_cache(csa, wl, dev, extra):
     """Fills every sequence's cache through the library's append (m = 1 here)."""
@@ -231,11 +245,7 @@ def run_csa2(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks.__exit__(None, None, None)
-    total = sum(times)
-    if world > 1:
-        t = torch.tensor([total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
+    total = job_time(sum(times), world, dev)
     assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
     ph /= args.steps
     if not ph_ok:
@@ -260,7 +270,7 @@ def run_csa2(args, rank, world):
                       wl.k * 4)
     attn_flops = B * 4 * wl.heads * 512 * (wl.k + wl.n_win)
     res = {
-        "metric": METRIC, "value": round(world * B * args.steps / total, 1), "unit": UNIT,
+        "metric": METRIC, "value": round(job_value(B * args.steps, world, total), 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (indexer MMA), fp4/bf16 -> fp32 (attention)",
         "data": "synthetic (seeded counter-hash generator; N(0,1) latents scaled to norm sqrt(512))",
@@ -322,13 +332,9 @@ def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
         torch.cuda.synchronize()
         if s >= args.warmup:
             times.append(e0.elapsed_time(e1) / 1e3)
-    total = sum(times)
-    if world > 1:
-        t = torch.tensor([total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
+    total = job_time(sum(times), world, dev)
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    return {"value": round(world * B * args.steps / total, 1), "unit": UNIT,
+    return {"value": round(job_value(B * args.steps, world, total), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 4,
             "ms_per_step": round(total / args.steps * 1e3, 4)}
 

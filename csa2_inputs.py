@@ -16,7 +16,9 @@ Value recipes (workload shapes follow the pages' decode and prefill settings):
   attention queries q: ~N(0, 1/512), rounded to bf16;
   window KV: ~N(0, 1), rounded to bf16;
   exact-integer mode: keys and queries integers in [-8, 8], w in multiples of
-      1/16, so every fp32 product and partial sum of the indexer is exact.
+      1/16, so every fp32 product and partial sum of the indexer is exact;
+  exact-compression mode (m > 1): latents on a 2^-10 grid in [-8, 8] and Z
+      equal within each block, so the block average is exact in fp32.
 """
 from __future__ import annotations
 
@@ -83,14 +85,16 @@ def normal(shape, seed, stream, device="cpu", start=0) -> torch.Tensor:
     """~N(0, 1): (sum of four 16-bit uniforms - 2) * sqrt(3), fp32."""
     n = math.prod(shape)
 
-    def f(c):
-        acc = torch.zeros(c.shape, dtype=torch.float32, device=c.device)
-        for i in range(4):
-            u = (hash_u32(c * 4 + i, seed, stream) >> 16).to(torch.float32) * (1.0 / 65536.0)
-            acc = acc + u
-        return (acc - 2.0) * _SQRT3
+    return _gen(n, device, lambda c: _normal_of(c, seed, stream), torch.float32,
+                start).reshape(shape)
 
-    return _gen(n, device, f, torch.float32, start).reshape(shape)
+
+def _normal_of(c, seed, stream):
+    acc = torch.zeros(c.shape, dtype=torch.float32, device=c.device)
+    for i in range(4):
+        u = (hash_u32(c * 4 + i, seed, stream) >> 16).to(torch.float32) * (1.0 / 65536.0)
+        acc = acc + u
+    return (acc - 2.0) * _SQRT3
 
 
 def int_uniform(shape, lo, hi, seed, stream, device="cpu", start=0) -> torch.Tensor:
@@ -128,6 +132,8 @@ class Workload:
     n_win: int = 128         # sliding window
     pool_blocks: int = 2048  # candidate-pool blocks (8 positions each)
     exact: bool = False      # exact-integer indexer inputs
+    grid: bool = False       # latents on a 2^-10 grid (exact block sums)
+    equal_z: bool = False    # Z equal within each block (weights exactly 1/m)
     rms_norm: bool = False   # scale latents to norm sqrt(512)
     seed: int = 1000
     sm_scale: float = 1.0
@@ -145,11 +151,54 @@ def latent_rows(wl: Workload, b: int, p0: int, n: int, device):
     """C and Z of tokens p0..p0+n-1 of sequence b, [n][512] fp32 each (Z is
     None when m == 1)."""
     start = ((b << SEQ_SHIFT) + p0) * 512
-    C = normal((n, 512), wl.seed, S_C, device, start=start)
-    if wl.rms_norm:
-        C = rms_to_sqrt512(C)
-    Z = normal((n, 512), wl.seed, S_Z, device, start=start) if wl.m > 1 else None
+    if wl.grid:
+        C = _gen(n * 512, device, lambda c: _grid_of(c, wl.seed), torch.float32,
+                 start).reshape(n, 512)
+    else:
+        C = normal((n, 512), wl.seed, S_C, device, start=start)
+        if wl.rms_norm:
+            C = rms_to_sqrt512(C)
+    Z = None
+    if wl.m > 1:
+        if wl.equal_z:
+            Z = _gen(n * 512, device, lambda c: _equal_z(c, wl), torch.float32,
+                     start).reshape(n, 512)
+        else:
+            Z = normal((n, 512), wl.seed, S_Z, device, start=start)
     return C, Z
+
+
+def latent_rows_at(wl: Workload, b: int, entries, device="cpu"):
+    """C (and Z) of the tokens of the given entries of sequence b (entry e holds
+    tokens e*m .. e*m+m-1): [len(entries)][m][512] each, the same values
+    latent_rows gives for those tokens."""
+    e = torch.as_tensor(entries, dtype=torch.int64, device=device)
+    tok = (e[:, None] * wl.m + torch.arange(wl.m, device=device)[None]).reshape(-1)
+    cnt = (((b << SEQ_SHIFT) + tok) * 512)[:, None] + torch.arange(512, device=device)[None]
+    if wl.grid:
+        C = _grid_of(cnt, wl.seed)
+    else:
+        C = _normal_of(cnt, wl.seed, S_C)
+        if wl.rms_norm:
+            C = rms_to_sqrt512(C)
+    Z = None
+    if wl.m > 1:
+        Z = _equal_z(cnt, wl) if wl.equal_z else _normal_of(cnt, wl.seed, S_Z)
+        Z = Z.reshape(len(e), wl.m, 512)
+    return C.reshape(len(e), wl.m, 512), Z
+
+
+def _grid_of(cnt, seed):
+    """Multiples of 2^-10 in [-8, 8]: sums of two stay exact in fp32."""
+    return ((hash_u32(cnt, seed, S_C) >> 8) % 16385).to(torch.float32) * (1.0 / 1024.0) - 8.0
+
+
+def _equal_z(cnt, wl):
+    """Z equal over the m tokens of each entry (the weights are then exactly 1/m)."""
+    tok_cnt = cnt // 512
+    seq_part = tok_cnt - (tok_cnt % (1 << SEQ_SHIFT))
+    ent = seq_part + (tok_cnt % (1 << SEQ_SHIFT)) // wl.m
+    return _normal_of(ent * 512 + cnt % 512, wl.seed, S_Z)
 
 
 def key_rows(wl: Workload, b: int, e0: int, n: int, device):

@@ -127,12 +127,16 @@ double or_fp8_encode_vec(const double *x, int d, uint8_t *out)
 /* Batch form over fp32 input rows, for the tests. */
 void or_fp8_encode_rows(const float *x, int64_t rows, int d, uint8_t *out, float *scale)
 {
-    double *tmp = (double *)malloc(sizeof(double) * d);
-    for (int64_t r = 0; r < rows; ++r) {
-        for (int c = 0; c < d; ++c) tmp[c] = x[r * d + c];
-        scale[r] = (float)or_fp8_encode_vec(tmp, d, out + r * d);
+#pragma omp parallel
+    {
+        double *tmp = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            for (int c = 0; c < d; ++c) tmp[c] = x[r * d + c];
+            scale[r] = (float)or_fp8_encode_vec(tmp, d, out + r * d);
+        }
+        free(tmp);
     }
-    free(tmp);
 }
 
 /* ------------------------------------------------------------------------ */

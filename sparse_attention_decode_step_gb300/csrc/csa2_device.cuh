@@ -30,9 +30,18 @@ __device__ __forceinline__ uint32_t score_key(float f)
 }
 
 // ------------------------------------------------------------------ mbarrier
-// Waits give up after kSpinLimit polls (each poll may block for a short,
-// hardware-chosen time), so a broken pipeline returns instead of hanging.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Waits give up after kWaitNs nanoseconds of wall time (read from %globaltimer)
+// or kSpinLimit polls, whichever comes first, so a broken pipeline returns
+// with an error count instead of hanging the GPU.
+constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
@@ -73,13 +82,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Returns false when the wait gave up (limit reached or *abort set).
+// Returns false when the wait gave up (time or poll limit reached, or *abort set).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort_flag)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && *abort_flag) return false;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitNs) return false;
+        }
     }
     return false;
 }

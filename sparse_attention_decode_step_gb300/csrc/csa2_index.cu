@@ -20,7 +20,7 @@
 // TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
 // Units of work are (query group, 128-entry tile); each CTA takes a contiguous
 // range of units so the query tile (B operand) is reloaded only when the group
-// changes.  Every wait is bounded (csa2::kSpinLimit) and sets an abort flag.
+// changes.  Every wait is bounded in time (csa2::kWaitNs) and sets an abort flag.
 #include "csa2_device.cuh"
 #include "csa2_internal.h"
 
