@@ -175,6 +175,33 @@ csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_v
                       int32_t k, int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out,
                       void *workspace, size_t ws_bytes, void *stream);
 
+/* ---- 4b. top-k that allocates nothing ---------------------------------------
+ * The same selection as csa2_topk, for callers that cannot get device memory
+ * for a workspace: for instance a plugin running inside a host program that
+ * owns every device allocation, or a serving loop that forbids allocating once
+ * it has started.  The pages have no counterpart to this call; it is a
+ * convenience of this library.
+ *
+ * Scratch: a fixed 4 MiB array of device memory inside the library, held by
+ * every GPU that loads it until the process exits (its size is
+ * csa2_topk_noalloc_max_scratch()).  A problem whose
+ * csa2_topk_workspace_size(nq, max_n) exceeds it is refused with
+ * CSA2_ERR_CAPACITY and nothing is launched.  The call never allocates or
+ * frees memory.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture.  A failed lookup returns CSA2_ERR_CUDA.
+ * Sharing: every call on a device uses the same array, which keeps what the
+ * last call left in it (each call clears what it needs before use).  Calls
+ * whose kernels overlap on the GPU (different streams with no ordering) race
+ * on the array and give undefined results: order them on one stream.
+ * Arguments, outputs and errors are otherwise those of csa2_topk. */
+csa2_status csa2_topk_noalloc(const float *scores, int64_t ld_scores, const int32_t *n_valid,
+                              const int32_t *pool_blk, int32_t pool_blocks, int32_t nq,
+                              int64_t max_n, int32_t k, int32_t *idx_out, int64_t ld_idx,
+                              int32_t *cnt_out, void *stream);
+size_t csa2_topk_noalloc_max_scratch(void);
+
 /* ---- 5. candidate pool ----------------------------------------------------
  * From a Full layer's block maxima: the pool_blocks blocks with the largest
  * block max among the ceil(N_i / 8) visible blocks (ties to the lower block),

@@ -29,7 +29,8 @@ _STATUS = {0: "ok", -1: "invalid argument", -2: "pointer not 16-byte aligned",
 EXPORTS = ["csa2_quantize_append", "csa2_index_full", "csa2_index_reindex", "csa2_topk",
            "csa2_pool_select", "csa2_sparse_attn", "csa2_layer_step", "csa2_index_workspace_size",
            "csa2_topk_workspace_size", "csa2_attn_workspace_size", "csa2_layer_workspace_size",
-           "csa2_status_string", "csa2_launch_count"]
+           "csa2_status_string", "csa2_launch_count", "csa2_topk_noalloc",
+           "csa2_topk_noalloc_max_scratch"]
 
 
 class CsaError(RuntimeError):

@@ -11,6 +11,8 @@
 //
 // Pool ([Notes] section 3): the same selection over the block maxima of a Full
 // layer (k = 2,048 blocks), then the count of visible positions they hold.
+#include <mutex>
+
 #include "csa2_device.cuh"
 #include "csa2_internal.h"
 
@@ -389,3 +391,64 @@ cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_v
 }
 
 }  // namespace csa2
+
+// ---------------------------------------------------------------- allocation-free top-k
+// csa2_topk_noalloc keeps its scratch in a fixed array of device global memory
+// that lives as long as the library is loaded.  In host code the array's name
+// is only a stand-in, never a device address: the address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current.
+namespace csa2 {
+
+constexpr size_t kNoallocScratchBytes = 4u << 20;   // 4 MiB
+static __device__ __align__(256) uint8_t g_topk_scratch[kNoallocScratchBytes];
+
+static std::mutex g_scratch_mu;
+static void *g_scratch_addr[64] = {nullptr};
+
+// Device address of the scratch array on the current device; the first call
+// on a device looks it up.  nullptr if the lookup fails.
+static void *noalloc_scratch()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_topk_scratch) != cudaSuccess || ptr == nullptr)
+            return nullptr;
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace csa2
+
+extern "C" size_t csa2_topk_noalloc_max_scratch(void) { return csa2::kNoallocScratchBytes; }
+
+extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t ld_scores,
+                                         const int32_t *n_valid, const int32_t *pool_blk,
+                                         int32_t pool_blocks, int32_t nq, int64_t max_n, int32_t k,
+                                         int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out,
+                                         void *stream)
+{
+    using namespace csa2;
+    auto al = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    if (nq < 0) return CSA2_ERR_INVALID_ARG;
+    if (nq == 0) return CSA2_OK;
+    if (!scores || !n_valid || !idx_out || !cnt_out) return CSA2_ERR_INVALID_ARG;
+    if (!al(scores, 16) || !al(n_valid, 4) || !al(idx_out, 4) || !al(cnt_out, 4) ||
+        (pool_blk && !al(pool_blk, 4)))
+        return CSA2_ERR_ALIGN;
+    if (k < 1 || max_n < 1 || max_n >= (1LL << 31) || ld_scores < max_n || ld_scores % 4 != 0 ||
+        ld_idx < k)
+        return CSA2_ERR_INVALID_ARG;
+    if (pool_blk && (pool_blocks < 1 || max_n > 8LL * pool_blocks)) return CSA2_ERR_INVALID_ARG;
+    if (topk_workspace_bytes(nq, max_n) > kNoallocScratchBytes) return CSA2_ERR_CAPACITY;
+    void *scratch = noalloc_scratch();
+    if (scratch == nullptr) return CSA2_ERR_CUDA;
+    // launch_topk's first kernel clears the histograms and state it reads later
+    const cudaError_t e = launch_topk(scores, ld_scores, n_valid, 0, pool_blk, pool_blocks, nq,
+                                      max_n, k, idx_out, ld_idx, cnt_out, scratch,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
