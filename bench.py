@@ -166,7 +166,7 @@ def run_csa2(args, rank, world):
     B = wl.batch
     T0 = wl.ctx_tokens[0]
     n_steps = args.warmup + args.steps
-    cache = build_cache(csa, wl, dev, extra=2 * n_steps + 16)   # value steps + e2e steps
+    cache = build_cache(csa, wl, dev, extra=3 * n_steps + 16)   # value, phase and e2e steps
     wcap = 512
     win = ci.window_rows(wl, B, wcap, dev)          # ring buffers; every needed position filled
 
@@ -175,7 +175,7 @@ def run_csa2(args, rank, world):
     inputs = [step_inputs(wl, s, B, dev) for s in range(n_steps)]
     q_pos = torch.full((B,), T0, dtype=torch.int32, device=dev)
     qs = csa.Queries(list(range(B)), [T0] * B, 1, dev)
-    max_n = T0 + n_steps + 1
+    max_n = T0 + 2 * n_steps + 1
     ld = (max_n + 3) // 4 * 4
     scores = torch.empty(B, ld, device=dev)
     nv = torch.empty(B, dtype=torch.int32, device=dev)
@@ -191,35 +191,47 @@ def run_csa2(args, rank, world):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     outer = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
-    def phases():
-        ev[0].record()
+    def ph_append():
         csa.quantize_append(cache, stage["C"], None, stage["key"], counters=counters)
-        ev[1].record()
+
+    def ph_index():
         csa.index_full(cache, qs, stage["q_idx"], stage["w"], max_n, scores, n_valid=nv, ws=iws,
                        counters=counters)
-        ev[2].record()
+
+    def ph_topk():
         csa.topk(scores, nv, wl.k, idx, cnt, max_n=max_n, ws=tws)
-        ev[3].record()
+
+    def ph_attn():
         csa.sparse_attn(cache, qs, idx, cnt, stage["q"], win, wl.n_win, out, lse=lse,
                         ws=aws, counters=counters)
-        ev[4].record()
+
+    phase_fns = [ph_append, ph_index, ph_topk, ph_attn]
+    appended = [0]
 
     def load_step(s):
+        # step s appends the token at position T0 + (tokens appended so far)
         for k_ in stage:
-            stage[k_].copy_(inputs[s][k_])
-        qs.q_pos.fill_(T0 + s)
+            stage[k_].copy_(inputs[s % n_steps][k_])
+        qs.q_pos.fill_(T0 + appended[0])
+        appended[0] += 1
 
-    # capture one step as a CUDA graph (queries advance one position per step)
+    # one CUDA graph for the whole step, and one per phase (for the phase split)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     l0 = csa.launch_count()
     graph = torch.cuda.CUDAGraph()
-    # rows appended during capture must not count: the graph is captured, not run
     with torch.cuda.graph(graph, stream=side):
-        phases()
+        for f in phase_fns:
+            f()
     launches_per_step = csa.launch_count() - l0
+    pgraphs = []
+    for f in phase_fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            f()
+        pgraphs.append(g)
 
-    times, ph, ph_ok = [], np.zeros(4), True
+    times = []
     # clocks are sampled from the start of the warm-up to the end of the timed steps
     clocks = Clocks(torch.cuda.current_device()).__enter__()
     torch.cuda.synchronize()
@@ -237,27 +249,37 @@ def run_csa2(args, rank, world):
         if s >= args.warmup:
             torch.cuda.synchronize()
             times.append(outer[0].elapsed_time(outer[1]) / 1e3)
-            try:
-                ph += [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(4)]
-            except RuntimeError:
-                ph_ok = False
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks.__exit__(None, None, None)
     total = job_time(sum(times), world, dev)
-    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
-    ph /= args.steps
-    if not ph_ok:
-        ph = phase_times_eager(phases, ev, load_step, n_steps - 1)
     ms = total / args.steps * 1e3
+
+    # ---- phase split: the same steps with one graph per phase, events between them
+    ph = np.zeros(4)
+    n_ph = max(1, min(args.steps, 50))
+    entries_ph = 0
+    for s in range(n_ph):
+        load_step(s)
+        entries_ph += T0 + appended[0]            # visible entries after this step's append
+        flush.fill_(s & 0xFF)
+        torch.cuda.synchronize()
+        ev[0].record()
+        for i, g in enumerate(pgraphs):
+            g.replay()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        ph += [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(4)]
+    ph /= n_ph
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
 
     # ---- end to end: pinned host inputs in, output back, through the layer call
     e2e = run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world)
 
     # ---- roofline of the dominant kernel (Full-mode indexer)
     hbm, bf16, src = peaks()
-    entries = sum(T0 + args.warmup + s + 1 for s in range(args.steps)) / args.steps * B
+    entries = entries_ph / n_ph * B
     idx_bytes = entries * IDX_BYTES_PER_ENTRY
     achieved = idx_bytes / ph[1] / 1e9
     traffic = profiled_traffic()
@@ -291,16 +313,6 @@ def run_csa2(args, rank, world):
     return res
 
 
-def phase_times_eager(phases, ev, load_step, s):
-    """Phase durations from one eager (non-graph) run, when graph-captured
-    events cannot be timed."""
-    load_step(s)
-    torch.cuda.synchronize()
-    phases()
-    torch.cuda.synchronize()
-    return np.array([ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(4)])
-
-
 def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
     """Pinned host inputs -> device -> layer call -> output back to the host."""
     host = [{k_: v.cpu().pin_memory() for k_, v in step_inputs(wl, s, B, "cpu").items()}
@@ -311,7 +323,7 @@ def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
     cnt = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty(B, wl.heads, 512, device=dev)
     out_h = torch.empty(B, wl.heads, 512).pin_memory()
-    max_n = T0 + 2 * n_steps + 2
+    max_n = T0 + 3 * n_steps + 2
     layer = csa.Layer(csa.FULL, cache, qs, k=wl.k, q=dstage["q"], win=win, n_win=wl.n_win,
                       out=out, idx=idx, cnt=cnt, q_idx=dstage["q_idx"], w=dstage["w"], max_n=max_n)
     base_len = cache.seq_len.clone()
