@@ -55,12 +55,14 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the indexer from the committed ncu summary."""
+def profiled_bytes_per_entry():
+    """DRAM bytes per visible entry of the indexer kernel (read + write), from
+    the committed ncu summary of a smaller case of the same kernel; None if
+    there is none."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
     for line in open(PROFILE_SUMMARY):
-        if line.startswith("traffic_bytes_per_launch_scaled:"):
+        if line.startswith("dram_bytes_per_visible_entry:"):
             v = line.split(":", 1)[1].strip()
             return None if v in ("", "null") else float(v)
     return None
@@ -163,6 +165,9 @@ def run_csa2(args, rank, world):
     import sparse_attention_decode_step_gb300 as csa
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = ci.config(2)
+    if args.ctx:
+        wl.ctx_tokens = [args.ctx] * wl.batch
+        wl.name = f"decode_full_b{wl.batch}_ctx{args.ctx + 1}"
     B = wl.batch
     T0 = wl.ctx_tokens[0]
     n_steps = args.warmup + args.steps
@@ -275,18 +280,18 @@ def run_csa2(args, rank, world):
     assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
 
     # ---- end to end: pinned host inputs in, output back, through the layer call
-    e2e = run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world)
+    e2e = None if args.quick else run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world)
 
     # ---- roofline of the dominant kernel (Full-mode indexer)
     hbm, bf16, src = peaks()
     entries = entries_ph / n_ph * B
     idx_bytes = entries * IDX_BYTES_PER_ENTRY
     achieved = idx_bytes / ph[1] / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_bytes_per_entry()
     roof = {"kernel": "index_main_kernel (+ index_prep_kernel)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_source": src,
-            "traffic": None if traffic is None else round(traffic * entries / (B * 65536)),
+            "traffic": None if traffic is None else round(traffic * entries),
             "algorithmic_bytes_per_launch": round(idx_bytes)}
     attn_bytes = B * (wl.k * 288 + wl.n_win * 1024 + wl.heads * 512 * 2 + wl.heads * 512 * 4 +
                       wl.k * 4)
@@ -308,7 +313,7 @@ def run_csa2(args, rank, world):
         "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
-    if rank == 0:
+    if rank == 0 and not args.quick:
         res["cpu_baseline"] = cpu_baseline(wl, cache, win, inputs[args.warmup], T0 + args.warmup)
     return res
 
@@ -429,6 +434,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="profiling case: cached tokens per sequence instead of 65,535")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling case: skip the e2e and CPU-baseline legs")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
