@@ -17,8 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libcsa2.so")
 
-SOURCES = ["csa2_api.cu", "csa2_append.cu", "csa2_index.cu", "csa2_topk.cu", "csa2_attn_simt.cu",
-           "csa2_attn_tc.cu"]
+SOURCES = ["csa2_api.cu", "csa2_append.cu", "csa2_index.cu", "csa2_topk.cu", "csa2_attn_tc.cu"]
 HEADERS = ["csa2_device.cuh", "csa2_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-rdc=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -75,6 +75,7 @@ void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_s
     const int sms = device_sm_count();
     int s = sms / (nq > 0 ? nq : 1);
     if (s > tiles) s = tiles;
+    if (s > 152) s = 152;                  // the combine kernel holds at most 152 split weights
     if (s < 1) s = 1;
     const int tps = (tiles + s - 1) / s;
     *rows_per_split = tps * 128;

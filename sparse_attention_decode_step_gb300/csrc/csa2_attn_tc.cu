@@ -21,16 +21,19 @@
 // more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
 // in TMEM.
 //
-// Warps: 0 = MMA issuer / TMEM owner; 1..4 = row workers (thread = tile row:
-// gather + dequant, then softmax of that row; epilogue: thread = channel).
-// Partials (O unnormalised, reference max, sum) go to the workspace; the
-// split-combine kernel merges them.
+// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers, two per TMEM lane
+// quarter: a worker owns half of a tile row (256 channels to dequantise, 32
+// heads of its softmax; in the epilogue, 32 heads of one channel).  The
+// cross-row max reduction runs only when a logit exceeds its head's reference
+// max by more than 8 (always on the first tile); row sums are kept per thread
+// and reduced once.  Partials (O unnormalised [channel][head], reference max,
+// sum) go to the workspace; the combine kernel merges the splits.
 #include "csa2_device.cuh"
 #include "csa2_internal.h"
 
 namespace csa2 {
 
-constexpr int kTcThreads = 160;
+constexpr int kTcThreads = 288;       // warp 0 MMA, warps 1..8 workers
 constexpr int kRows = 128;           // rows per tile (MMA M)
 constexpr int kHeads = 64;           // MMA N (heads padded to 64)
 constexpr uint32_t kVBytes = kRows * CSA2_D * 2;          // 128 KB
@@ -155,13 +158,55 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Transposed warp reduction: 64 values per lane -> lane l holds the reduction
-// over the warp of values 2l and 2l+1 (in v[0], v[1]).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+{
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// 2^x (hardware approximation, relative error near 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Transposed warp reduction of 32 values per lane: afterwards lane l holds, in
+// v[0], the reduction over the warp's 32 lanes of value l.
 template <bool kMax>
-__device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane)
+__device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane)
 {
 #pragma unroll
-    for (int n = 64, o = 16; n > 2; n >>= 1, o >>= 1) {
+    for (int n = 32, o = 16; n > 1; n >>= 1, o >>= 1) {
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < n / 2; ++i) {
@@ -205,6 +250,13 @@ __device__ __forceinline__ TcRowSet tc_row_set(const AttnParams &p, int q)
     return rs;
 }
 
+constexpr int kWorkers = 256;                        // 8 worker warps, two per TMEM lane quarter
+
+__device__ __forceinline__ void named_sync_all_workers()
+{
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 {
     const int q = blockIdx.y, split = blockIdx.x;
@@ -217,14 +269,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     uint8_t *sV = smem;                       // [8 atoms][128 rows][128 B]
     uint8_t *sQ = sV + kVBytes;               // [8 atoms][64 heads][128 B]
     uint8_t *sP = sQ + kQBytes;               // [128 rows][64 heads] f16, 128 B rows
-    float *sRed = reinterpret_cast<float *>(sP + kPBytes);   // [4][64]
+    float *sRed = reinterpret_cast<float *>(sP + kPBytes);   // [4 quarters][64 heads]
     float *sM = sRed + 4 * 64;                // reference max per head (log2 units)
-    float *sL = sM + 64;                      // running sum per head
-    float *sAlpha = sL + 64;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sAlpha + 64);
+    float *sAlpha = sM + 64;                  // rescale factor of the current tile
+    float *sL = sAlpha + 64;                  // running sum per head
+    float *sRedL = sL + 64;                   // [4 quarters][64 heads] tile row sums
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRedL + 4 * 64);
     uint64_t *bar_v = bars, *bar_s = bars + 1, *bar_p = bars + 2, *bar_o = bars + 3;
-    uint64_t *bar_done = bars + 4;
-    int *sFlag = reinterpret_cast<int *>(bars + 5);          // [0] abort, [1] rescale, [2] bad
+    uint64_t *bar_done = bars + 4, *bar_q = bars + 5;
+    int *sFlag = reinterpret_cast<int *>(bars + 6);   // [0] abort [1] rescale [2] bad [3] need max
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sFlag + 4);
     volatile int *abort_flag = sFlag;
 
@@ -235,27 +288,117 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int n_tiles = (r_end > r_begin) ? (r_end - r_begin + kRows - 1) / kRows : 0;
 
     if (tid == 0) {
-        mbar_init(bar_v, 4);
+        mbar_init(bar_v, kWorkers / 32);
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 4);
+        mbar_init(bar_p, kWorkers / 32);
         mbar_init(bar_o, 1);
         mbar_init(bar_done, 1);
+        mbar_init(bar_q, 1);
         sFlag[0] = 0;
         sFlag[1] = 0;
         sFlag[2] = rs.bad ? 1 : 0;
+        sFlag[3] = 0;
         fence_barrier_init();
     }
-    if (tid < 64) { sM[tid] = -INFINITY; sL[tid] = 0.f; sAlpha[tid] = 1.f; }
+    if (tid < 64) { sM[tid] = -INFINITY; sAlpha[tid] = 1.f; sL[tid] = 0.f; }
     if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
 
-    // ---- Q: bf16 -> f16, K-major 128-byte swizzle, heads >= H are zero
+    // ---- Q: one bulk copy of the raw bf16 block [H][512] into the (still free)
+    // V tile, then bf16 -> f16 into the K-major 128-byte-swizzled sQ; heads >= H are zero
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t qbytes = (uint32_t)H * CSA2_D * 2;
+        mbar_arrive_expect_tx(bar_q, qbytes);
+        bulk_load(sV, p.q + (int64_t)q * H * CSA2_D, qbytes, bar_q);
+    }
+    // the worker threads start gathering the first tile's rows meanwhile (below)
+    const int wt = tid - 32;                          // worker index 0..255
+    const uint32_t quarter = (uint32_t)(warp & 3);    // TMEM lanes 32 quarter ..
+    const int row = (int)(quarter * 32 + lane);       // tile row == TMEM lane of this thread
+    const int half = (warp - 1) >> 2;                 // channels 256 half .., heads 32 half ..
+    uint4 rc[8], rsc;                                 // half an FP4 row: 128 B codes + 16 B scales
+    int kind = 0;                                     // 0 empty, 1 fp4, 2 window
+    int64_t wrow = 0;
+    int next_j = -1;
+    auto entry_of = [&](int tile) -> int {
+        const int g = r_begin + tile * kRows + row;
+        return (g < r_end && g < rs.cnt) ? p.idx[(int64_t)q * p.ld_idx + g] : -1;
+    };
+    auto fetch = [&](int tile, int j) {
+        const int g = r_begin + tile * kRows + row;
+        kind = 0;
+        if (g < r_end) {
+            if (g < rs.cnt) {
+                if (j >= 0 && j < rs.nt) {
+                    kind = 1;
+                    const int64_t r = rs.base + j;
+                    const uint4 *c4 = reinterpret_cast<const uint4 *>(
+                        p.codes + r * CSA2_CODE_BYTES + half * (CSA2_CODE_BYTES / 2));
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) rc[k] = __ldg(c4 + k);
+                    rsc = __ldg(reinterpret_cast<const uint4 *>(p.scales + r * CSA2_SCALE_BYTES) + half);
+                } else {
+                    sFlag[2] = 1;
+                }
+            } else {
+                kind = 2;
+                const int64_t pos = rs.lo + (g - rs.cnt);
+                wrow = ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D + half * (CSA2_D / 2);
+            }
+        }
+    };
+    // dequantise (or copy) this thread's half row into the f16 V tile
+    auto store_v = [&]() {
+        if (kind == 1) {
+            const uint32_t sw[4] = {rsc.x, rsc.y, rsc.z, rsc.w};   // 16 scale bytes
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {                // atom column 4 half + a
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {            // 8 channels = 4 code bytes
+                    const int word = a * 8 + c;
+                    const uint4 &u = rc[word >> 2];
+                    const uint32_t w = (word & 3) == 0 ? u.x : (word & 3) == 1 ? u.y
+                                     : (word & 3) == 2 ? u.z : u.w;
+                    const int grp = (64 * a + 8 * c) >> 4;       // scale group within the half
+                    const uint32_t sb = (sw[grp >> 2] >> (8 * (grp & 3))) & 0xFFu;
+                    *reinterpret_cast<uint4 *>(sV + (4 * half + a) * kVAtom + sw128(row, c)) =
+                        fp4x8_to_f16(w, scale_pair(sb));
+                }
+            }
+        } else if (kind == 2) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.win + wrow);
+#pragma unroll 1
+            for (int b16 = 0; b16 < 2; ++b16) {          // 2 batches of 16 loads in flight
+                uint4 raw[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) raw[k] = __ldg(src + 16 * b16 + k);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int kk = 16 * b16 + k;         // 16-byte chunk of the half row
+                    *reinterpret_cast<uint4 *>(sV + (4 * half + (kk >> 3)) * kVAtom + sw128(row, kk & 7)) =
+                        make_uint4(bf16x2_to_f16x2(raw[k].x), bf16x2_to_f16x2(raw[k].y),
+                                   bf16x2_to_f16x2(raw[k].z), bf16x2_to_f16x2(raw[k].w));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                *reinterpret_cast<uint4 *>(sV + (4 * half + (k >> 3)) * kVAtom + sw128(row, k & 7)) =
+                    make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (warp > 0 && n_tiles > 0) {
+        fetch(0, entry_of(0));
+        if (n_tiles > 1) next_j = entry_of(1);
+    }
     {
-        const uint16_t *qg = p.q + (int64_t)q * H * CSA2_D;
+        volatile int no_abort = 0;
+        if (!mbar_wait(bar_q, 0, &no_abort)) sFlag[0] = 1;
         for (int i = tid; i < kHeads * (CSA2_D / 8); i += kTcThreads) {
             const int h = i / (CSA2_D / 8), c8 = i % (CSA2_D / 8);   // 8 channels per chunk
             uint4 v = make_uint4(0, 0, 0, 0);
             if (h < H) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qg + h * CSA2_D + c8 * 8));
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sV + h * 1024 + c8 * 16);
                 v = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
                                bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
             }
@@ -309,76 +452,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             mbar_wait(bar_done, 0, &no_abort);
         }
     } else {
-        // ============================================== row workers (128 threads)
-        const int t = tid - 32;                           // tile row / TMEM lane in softmax
-        const uint32_t quarter = (uint32_t)(warp & 3);   // TMEM lanes 32 quarter ..
-        const int row = (int)(quarter * 32 + lane);      // TMEM lane owned by this thread
+        // ============================================== 8 worker warps
         const float l2s = p.sm_scale * 1.4426950408889634f;
-        // prefetch registers: one FP4 row (256 B codes + 32 B scales)
-        uint4 rc[16], rsc[2];
-        int kind = 0;                                    // 0 empty, 1 fp4, 2 window
-        int64_t wrow = 0;
-        auto fetch = [&](int tile) {
-            const int g = r_begin + tile * kRows + row;
-            kind = 0;
-            if (g < r_end) {
-                if (g < rs.cnt) {
-                    const int j = p.idx[(int64_t)q * p.ld_idx + g];
-                    if (j >= 0 && j < rs.nt) {
-                        kind = 1;
-                        const int64_t r = rs.base + j;
-                        const uint4 *c4 = reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES);
-                        const uint4 *s4 = reinterpret_cast<const uint4 *>(p.scales + r * CSA2_SCALE_BYTES);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) rc[k] = __ldg(c4 + k);
-                        rsc[0] = __ldg(s4);
-                        rsc[1] = __ldg(s4 + 1);
-                    } else {
-                        sFlag[2] = 1;
-                    }
-                } else {
-                    kind = 2;
-                    const int64_t pos = rs.lo + (g - rs.cnt);
-                    wrow = ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D;
-                }
-            }
-        };
-        auto store_v = [&]() {
-            if (kind == 1) {
-                const uint32_t sw[8] = {rsc[0].x, rsc[0].y, rsc[0].z, rsc[0].w,
-                                        rsc[1].x, rsc[1].y, rsc[1].z, rsc[1].w};
-#pragma unroll
-                for (int a = 0; a < 8; ++a) {            // atom column: channels 64a..64a+63
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {        // 8 channels = 4 code bytes
-                        const int word = a * 8 + c;      // 32-bit word of the codes
-                        const uint4 &u = rc[word >> 2];
-                        const uint32_t w = (word & 3) == 0 ? u.x : (word & 3) == 1 ? u.y
-                                         : (word & 3) == 2 ? u.z : u.w;
-                        const int grp = (64 * a + 8 * c) >> 4;       // scale group
-                        const uint32_t sb = (sw[grp >> 2] >> (8 * (grp & 3))) & 0xFFu;
-                        *reinterpret_cast<uint4 *>(sV + a * kVAtom + sw128(row, c)) =
-                            fp4x8_to_f16(w, scale_pair(sb));
-                    }
-                }
-            } else if (kind == 2) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.win + wrow);
-#pragma unroll 4
-                for (int k = 0; k < 64; ++k) {
-                    const uint4 raw = __ldg(src + k);
-                    *reinterpret_cast<uint4 *>(sV + (k >> 3) * kVAtom + sw128(row, k & 7)) =
-                        make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
-                                   bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 64; ++k)
-                    *reinterpret_cast<uint4 *>(sV + (k >> 3) * kVAtom + sw128(row, k & 7)) =
-                        make_uint4(0, 0, 0, 0);
-            }
-        };
-
-        if (n_tiles > 0) fetch(0);
+        const int h0 = 32 * half;                      // this thread's heads h0 .. h0+31
         bool ok = true;
         for (int i = 0; i < n_tiles && ok; ++i) {
             if (i > 0) {
@@ -391,118 +467,149 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_v);
-            if (i + 1 < n_tiles) fetch(i + 1);
+            if (i + 1 < n_tiles) {
+                fetch(i + 1, next_j);
+                if (i + 2 < n_tiles) next_j = entry_of(i + 2);
+            }
 
-            // ---- softmax of this thread's row
+            // ---- softmax of this row, heads h0 .. h0+31
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            float x[64];
-            tmem_ld64(tS + ((quarter * 32u) << 16), x);
+            float x[32];
+            tmem_ld32(tS + ((quarter * 32u) << 16) + (uint32_t)h0, x);
             tmem_wait_ld();
+            bool over = false;
 #pragma unroll
-            for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * l2s : -INFINITY;
-            float r[64];
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 m4 = reinterpret_cast<const float4 *>(sM + h0)[h4];
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int h = 0; h < 64; ++h) r[h] = x[h];
-            warp_reduce64<true>(r, lane);
-            sRed[quarter * 64 + 2 * lane] = r[0];
-            sRed[quarter * 64 + 2 * lane + 1] = r[1];
-            named_sync_workers();
-            if (t < 64) {
-                const float tmax = fmaxf(fmaxf(sRed[t], sRed[64 + t]), fmaxf(sRed[128 + t], sRed[192 + t]));
-                const float m_old = sM[t];
-                float alpha = 1.f;
-                if (tmax > m_old + kRescaleThreshold || (m_old == -INFINITY && tmax > -INFINITY)) {
-                    alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - tmax);
-                    sM[t] = tmax;
-                    if (i > 0) sFlag[1] = 1;
+                for (int j = 0; j < 4; ++j) {
+                    const int h = 4 * h4 + j;
+                    x[h] = valid ? x[h] * l2s : -INFINITY;
+                    over |= x[h] > mm[j] + kRescaleThreshold;
                 }
-                sAlpha[t] = alpha;
             }
-            named_sync_workers();
-            // P = 2^(x - m) as f16 into sP (row = this thread's tile row)
-            float mh[64];
+            // the reference max moves only when some logit is more than 8 above it;
+            // the flag holds the number of the last tile that needed it (no reset)
+            if (over) sFlag[3] = i + 1;
+            named_sync_all_workers();
+            const bool need_max = sFlag[3] == i + 1;
+            if (need_max) {
+                float r[32];
 #pragma unroll
-            for (int h4 = 0; h4 < 16; ++h4) {
-                const float4 m4 = reinterpret_cast<const float4 *>(sM)[h4];
-                mh[4 * h4] = m4.x; mh[4 * h4 + 1] = m4.y; mh[4 * h4 + 2] = m4.z; mh[4 * h4 + 3] = m4.w;
+                for (int h = 0; h < 32; ++h) r[h] = x[h];
+                warp_reduce32<true>(r, lane);
+                sRed[quarter * 64 + h0 + lane] = r[0];
+                named_sync_all_workers();
+                if (wt < 64) {
+                    const float tmax = fmaxf(fmaxf(sRed[wt], sRed[64 + wt]),
+                                             fmaxf(sRed[128 + wt], sRed[192 + wt]));
+                    const float m_old = sM[wt];
+                    float alpha = 1.f;
+                    if (tmax > m_old + kRescaleThreshold) {
+                        alpha = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - tmax);
+                        sM[wt] = tmax;
+                        sL[wt] *= alpha;
+                        if (i > 0) sFlag[1] = 1;
+                    }
+                    sAlpha[wt] = alpha;
+                }
+                named_sync_all_workers();
+                const bool rescale = sFlag[1] != 0;
+                if (rescale) {
+                    // O^T *= alpha per head; PV of the previous tile has completed
+                    float al[32];
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; ++h4) {
+                        const float4 a4 = reinterpret_cast<const float4 *>(sAlpha + h0)[h4];
+                        al[4 * h4] = a4.x; al[4 * h4 + 1] = a4.y; al[4 * h4 + 2] = a4.z; al[4 * h4 + 3] = a4.w;
+                    }
+#pragma unroll 1
+                    for (int mb = 0; mb < 4; ++mb) {
+                        float o[32];
+                        const uint32_t ta = tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16);
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) o[h] *= al[h];
+                        tmem_st32(ta, o);
+                    }
+                    tmem_wait_st();
+                }
+                named_sync_all_workers();
+                if (wt == 0) sFlag[1] = 0;
+            }
+            // P = 2^(x - m) as f16 into sP; the row sums stay in registers
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 m4 = reinterpret_cast<const float4 *>(sM + h0)[h4];
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int h = 4 * h4 + j;
+                    x[h] = (mm[j] == -INFINITY) ? 0.f : fast_exp2(x[h] - mm[j]);
+                }
             }
 #pragma unroll
-            for (int h = 0; h < 64; ++h) x[h] = (mh[h] == -INFINITY) ? 0.f : exp2f(x[h] - mh[h]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 const uint4 v = make_uint4(f32x2_to_f16x2(x[8 * c], x[8 * c + 1]),
                                            f32x2_to_f16x2(x[8 * c + 2], x[8 * c + 3]),
                                            f32x2_to_f16x2(x[8 * c + 4], x[8 * c + 5]),
                                            f32x2_to_f16x2(x[8 * c + 6], x[8 * c + 7]));
-                *reinterpret_cast<uint4 *>(sP + sw128(row, c)) = v;
-            }
-            warp_reduce64<false>(x, lane);
-            sRed[quarter * 64 + 2 * lane] = x[0];
-            sRed[quarter * 64 + 2 * lane + 1] = x[1];
-            named_sync_workers();
-            if (t < 64) sL[t] = sL[t] * sAlpha[t] + ((sRed[t] + sRed[64 + t]) + (sRed[128 + t] + sRed[192 + t]));
-            const bool rescale = sFlag[1] != 0;
-            named_sync_workers();
-            if (rescale) {
-                // O^T *= alpha per head (column); PV of the previous tile has completed
-                float al[64];
-#pragma unroll
-                for (int h4 = 0; h4 < 16; ++h4) {
-                    const float4 a4 = reinterpret_cast<const float4 *>(sAlpha)[h4];
-                    al[4 * h4] = a4.x; al[4 * h4 + 1] = a4.y; al[4 * h4 + 2] = a4.z; al[4 * h4 + 3] = a4.w;
-                }
-#pragma unroll 1
-                for (int mb = 0; mb < 4; ++mb) {
-                    float o[64];
-                    const uint32_t ta = tO + 64 * mb + ((quarter * 32u) << 16);
-                    tmem_ld64(ta, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int h = 0; h < 64; ++h) o[h] *= al[h];
-                    tmem_st64(ta, o);
-                }
-                tmem_wait_st();
-                named_sync_workers();
-                if (t == 0) sFlag[1] = 0;
+                *reinterpret_cast<uint4 *>(sP + sw128(row, 4 * half + c)) = v;
             }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p);
+            // this tile's row sums: over the warp's 32 rows, then the 4 quarters
+            warp_reduce32<false>(x, lane);
+            sRedL[quarter * 64 + h0 + lane] = x[0];
+            named_sync_all_workers();
+            if (wt < 64)
+                sL[wt] += (sRedL[wt] + sRedL[64 + wt]) + (sRedL[128 + wt] + sRedL[192 + wt]);
         }
         if (!ok) *abort_flag = 1;
+        named_sync_all_workers();
 
-        // ---- epilogue: O^T (unnormalised) -> partials; thread = channel within block
+        // ---- epilogue: O^T (unnormalised) -> partials [split][channel][head]
         if (ok && n_tiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
             tc_fence_after();
         }
-        const int64_t pbase = ((int64_t)q * p.splits + split) * H;
+        const int64_t pbase = (int64_t)q * p.splits + split;
         if (ok) {
-            float *po = p.part_o + pbase * CSA2_D;
+            float *po = p.part_o + pbase * CSA2_D * H;
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
-                float o[64];
+                float o[32];
                 if (n_tiles > 0) {
-                    tmem_ld64(tO + 64 * mb + ((quarter * 32u) << 16), o);
+                    tmem_ld32(tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16), o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int h = 0; h < 64; ++h) o[h] = 0.f;
+                    for (int h = 0; h < 32; ++h) o[h] = 0.f;
                 }
-                const int c = 128 * mb + row;
+                float *dst = po + (int64_t)(128 * mb + row) * H + h0;
+                if (h0 + 32 <= H) {
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    if (h < H) po[(int64_t)h * CSA2_D + c] = o[h];
+                    for (int h4 = 0; h4 < 8; ++h4)
+                        reinterpret_cast<float4 *>(dst)[h4] =
+                            make_float4(o[4 * h4], o[4 * h4 + 1], o[4 * h4 + 2], o[4 * h4 + 3]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h)
+                        if (h0 + h < H) dst[h] = o[h];
+                }
             }
-            if (t < H) {
-                p.part_ml[(pbase + t) * 2] = (n_tiles > 0) ? sM[t] : -INFINITY;
-                p.part_ml[(pbase + t) * 2 + 1] = (n_tiles > 0) ? sL[t] : 0.f;
+            if (wt < H) {
+                p.part_ml[(pbase * H + wt) * 2] = (n_tiles > 0) ? sM[wt] : -INFINITY;
+                p.part_ml[(pbase * H + wt) * 2 + 1] = (n_tiles > 0) ? sL[wt] : 0.f;
             }
         }
-        if (t == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+        if (wt == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
     }
 
     tc_fence_before();
@@ -513,12 +620,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     }
 }
 
+// Merges the splits of each query: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
+// lse = (M + log2 L) ln 2.  Block = (query, 32 channels); partials [split][channel][head].
+// The per-split weights are computed once into shared memory; every thread then
+// sums its elements over the splits with independent loads.
+constexpr int kCombineMaxSplits = 152;   // static shared memory stays under 48 KB
+
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p)
+{
+    const int q = blockIdx.y, c0 = blockIdx.x * 32;
+    const int H = p.H, tid = threadIdx.x, S = p.splits;
+    __shared__ float sW[kCombineMaxSplits][64];   // weight of split s for head h
+    __shared__ float sInv[64];
+    __shared__ float sOut[32][65];                // [channel][head]
+    const float *ml = p.part_ml + (int64_t)q * S * H * 2;
+    if (tid < H) {
+        float M = -INFINITY;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((int64_t)s * H + tid) * 2]);
+        float L = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float ms = ml[((int64_t)s * H + tid) * 2];
+            const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+            sW[s][tid] = w;
+            L = fmaf(ml[((int64_t)s * H + tid) * 2 + 1], w, L);
+        }
+        sInv[tid] = (L > 0.f) ? 1.f / L : 0.f;
+        if (p.lse != nullptr && blockIdx.x == 0)
+            p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    const float *src = p.part_o + ((int64_t)q * S * CSA2_D + c0) * H;   // split 0, channel c0
+    const int64_t split_stride = (int64_t)CSA2_D * H;
+    for (int e = tid; e < 32 * H; e += 256) {
+        const int h = e % H;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int s = 0;
+        for (; s + 4 <= S; s += 4) {
+            a0 = fmaf(__ldg(src + (s + 0) * split_stride + e), sW[s + 0][h], a0);
+            a1 = fmaf(__ldg(src + (s + 1) * split_stride + e), sW[s + 1][h], a1);
+            a2 = fmaf(__ldg(src + (s + 2) * split_stride + e), sW[s + 2][h], a2);
+            a3 = fmaf(__ldg(src + (s + 3) * split_stride + e), sW[s + 3][h], a3);
+        }
+        for (; s < S; ++s) a0 = fmaf(__ldg(src + s * split_stride + e), sW[s][h], a0);
+        sOut[e / H][h] = ((a0 + a1) + (a2 + a3)) * sInv[h];
+    }
+    __syncthreads();
+    for (int i = tid; i < 32 * H; i += 256) {      // out[q][h][c0 + c]: 32 channels per head
+        const int h = i / 32, c = i % 32;
+        p.out[((int64_t)q * H + h) * CSA2_D + c0 + c] = sOut[c][h];
+    }
+}
+
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
-    const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (4 * 64 + 3 * 64) * 4 + 5 * 8 + 64;
+    const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 + 6 * 8 + 64;
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attn_tc_kernel<<<dim3(p.splits, p.nq), kTcThreads, smem, st>>>(p);
-    attn_combine_kernel<<<dim3(p.H, p.nq), 128, 0, st>>>(p);
+    attn_combine_kernel<<<dim3(CSA2_D / 32, p.nq), 256, 0, st>>>(p);
     note_launch(2);
     return cudaGetLastError();
 }

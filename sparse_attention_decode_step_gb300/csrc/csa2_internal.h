@@ -65,7 +65,7 @@ struct AttnParams {
     int n_win;
     float sm_scale;
     float *out, *lse;
-    float *part_o;      // [nq][splits][H][512]
+    float *part_o;      // [nq][splits][512][H]
     float *part_ml;     // [nq][splits][H][2]
     int splits, rows_per_split;
     uint32_t *counters;
@@ -74,8 +74,6 @@ struct AttnParams {
 // Splits of the row set and the workspace they need.
 void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_split);
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win);
-cudaError_t launch_attn_simt(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
-__global__ void attn_combine_kernel(AttnParams p);
 
 }  // namespace csa2

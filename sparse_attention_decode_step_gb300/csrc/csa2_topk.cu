@@ -11,6 +11,7 @@
 //
 // Pool ([Notes] section 3): the same selection over the block maxima of a Full
 // layer (k = 2,048 blocks), then the count of visible positions they hold.
+#include <cooperative_groups.h>
 #include <mutex>
 
 #include "csa2_device.cuh"
@@ -38,6 +39,7 @@ struct TopkParams {
     const int32_t *pool_blk;    // candidate -> position map, or null
     int pool_blocks;
     int nq, k, n_chunks;
+    int64_t max_n;              // bound on every query's candidate count (smem sizing)
     int32_t *idx_out;
     int64_t ld_idx;
     int32_t *cnt_out;
@@ -304,6 +306,185 @@ __global__ void __launch_bounds__(kTkThreads) topk_write_kernel(TopkParams p)
     }
 }
 
+// ---------------------------------------------------------------- one cluster per query
+// Up to kClusterMax candidates: a cluster of 8 CTAs per query.  Each CTA keeps
+// its eighth of the keys in shared memory (one pass over the scores) and
+// builds a shared-memory histogram of each round; the non-empty bins go to the
+// query's histogram in the workspace with global atomics, and after a cluster
+// barrier every CTA reads it back and takes the same digit decision.  The
+// ordered compaction exchanges per-CTA counts the same way.  One launch; the
+// cluster barriers are hardware barriers reached by every CTA equally often.
+constexpr int kClusterCtas = 8;
+constexpr int kClThreads = 512;
+constexpr int64_t kClusterMax = 262144;
+constexpr int kClChunkMax = (int)(kClusterMax / kClusterCtas);   // keys per CTA
+
+// Block-wide exclusive scan (512 threads); *total gets the block sum.
+__device__ __forceinline__ uint32_t scan512(uint32_t v, uint32_t *s_warp, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < kClThreads / 32 ? s_warp[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kClThreads / 32) s_warp[lane] = w;       // inclusive warp totals
+    }
+    __syncthreads();
+    const uint32_t before = warp > 0 ? s_warp[warp - 1] : 0u;
+    if (total) *total = s_warp[kClThreads / 32 - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThreads)
+    topk_cluster_kernel(TopkParams p)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int q = blockIdx.y, rank = (int)cluster.block_rank(), tid = threadIdx.x;
+    extern __shared__ __align__(16) uint32_t s_keys[];          // [chunk]
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t s_warp[kClThreads / 32];
+    __shared__ uint32_t s_digit, s_above;
+
+    int n = p.n_valid[q];
+    if (p.n_div8) n = (n + 7) / 8;
+    if (n < 0) n = 0;
+    if (n > p.max_n) n = (int)p.max_n;                           // shared memory was sized for max_n
+    const int chunk = ((n + kClusterCtas - 1) / kClusterCtas + 3) & ~3;
+    const int lo = min(rank * chunk, n), hi = min(lo + chunk, n);
+    const int len = hi - lo;
+    const float *row = p.scores + (int64_t)q * p.ld;
+    const bool all = n <= p.k;
+    uint32_t prefix = 0;
+    int32_t k_rem = all ? n : p.k;
+    // per-query global histograms (one per round) and per-CTA counts, in the workspace
+    uint32_t *ghist = p.hist + (int64_t)q * 3 * kBins;
+    uint32_t *gcnt = p.ccount + (int64_t)q * kClusterCtas * 2;
+    if (rank == 0) {
+        if (tid == 0) p.cnt_out[q] = all ? n : p.k;
+        for (int i = tid; i < 3 * kBins; i += kClThreads) ghist[i] = 0u;
+    }
+
+    // keys of this CTA's candidates into shared memory (lo is a multiple of 4)
+    for (int i = tid * 4; i < len; i += kClThreads * 4) {
+        if (i + 4 <= len) {
+            const float4 f = *reinterpret_cast<const float4 *>(row + lo + i);
+            s_keys[i] = score_key(f.x);
+            s_keys[i + 1] = score_key(f.y);
+            s_keys[i + 2] = score_key(f.z);
+            s_keys[i + 3] = score_key(f.w);
+        } else {
+            for (int j = i; j < len; ++j) s_keys[j] = score_key(row[lo + j]);
+        }
+    }
+    cluster.sync();                                              // histograms zeroed, keys loaded
+
+    if (!all) {
+        for (int r = 0; r < 3; ++r) {
+            const int sh = r == 0 ? 21 : (r == 1 ? 10 : 0);
+            const int pbits = r == 0 ? 0 : (r == 1 ? 11 : 22);
+            const uint32_t nb = r == 2 ? 1024u : 2048u;
+            for (int i = tid; i < kBins; i += kClThreads) hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < len; i += kClThreads) {
+                const uint32_t key = s_keys[i];
+                if (r == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1u)], 1u);
+            }
+            __syncthreads();
+            uint32_t *gh = ghist + r * kBins;
+            for (int i = tid; i < (int)nb; i += kClThreads)
+                if (hist[i]) atomicAdd(gh + i, hist[i]);
+            cluster.sync();                                      // the query's histogram is complete
+            // digit d with count(> d) < k_rem <= count(>= d); bins from the top, 4 per thread
+            uint32_t c[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int b = kBins - 1 - tid * 4 - j;
+                c[j] = b < (int)nb ? __ldcg(gh + b) : 0u;
+            }
+            if (tid == 0) { s_digit = 0; s_above = 0; }
+            const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+            const uint32_t before = scan512(mine, s_warp, nullptr);
+            const uint32_t need = (uint32_t)k_rem;
+            if (before < need && need <= before + mine) {
+                uint32_t acc = before;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (need <= acc + c[j]) { s_digit = kBins - 1 - tid * 4 - j; s_above = acc; break; }
+                    acc += c[j];
+                }
+            }
+            __syncthreads();
+            prefix = (prefix << (r == 2 ? 10 : 11)) | s_digit;
+            k_rem -= (int32_t)s_above;
+        }
+    }
+
+    // ---- ordered compaction: keys > T, then the lowest-position keys == T
+    const uint32_t T = prefix;
+    uint32_t gt = 0, eq = 0;
+    for (int i = tid; i < len; i += kClThreads) {
+        const uint32_t key = s_keys[i];
+        gt += all || key > T;
+        eq += !all && key == T;
+    }
+    uint32_t gt_tot, eq_tot;
+    scan512(gt, s_warp, &gt_tot);
+    scan512(eq, s_warp, &eq_tot);
+    if (tid == 0) { gcnt[2 * rank] = gt_tot; gcnt[2 * rank + 1] = eq_tot; }
+    cluster.sync();
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int rr = 0; rr < rank; ++rr) {
+        gt_before += __ldcg(gcnt + 2 * rr);
+        eq_before += __ldcg(gcnt + 2 * rr + 1);
+    }
+    uint32_t out_base = gt_before + min(eq_before, (uint32_t)(all ? 0 : k_rem));
+    uint32_t eq_base = eq_before;
+    int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
+    const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
+    for (int c0 = 0; c0 < len; c0 += kClThreads * 4) {
+        const int i0 = c0 + tid * 4;
+        uint32_t sel = 0, eqm = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j < len) {
+                const uint32_t key = s_keys[i0 + j];
+                if (all || key > T) sel |= 1u << j;
+                else if (key == T) eqm |= 1u << j;
+            }
+        }
+        uint32_t et, ot;
+        uint32_t er = eq_base + scan512(__popc(eqm), s_warp, &et);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (eqm & (1u << j)) { if ((int32_t)er < k_rem) sel |= 1u << j; ++er; }
+        uint32_t slot = out_base + scan512(__popc(sel), s_warp, &ot);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (sel & (1u << j)) {
+                const int64_t ii = lo + i0 + j;
+                const int32_t pos = pb ? 8 * pb[ii >> 3] + (int32_t)(ii & 7) : (int32_t)ii;
+                if (slot < (uint32_t)p.k) out[slot] = pos;
+                ++slot;
+            }
+        }
+        eq_base += et;
+        out_base += ot;
+    }
+}
+
 // Pool size: 8 per chosen block, minus the invisible tail of the newest block
 // when it is partial and was chosen.
 __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
@@ -325,7 +506,8 @@ __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_bl
 // ---------------------------------------------------------------- host side
 size_t topk_workspace_bytes(int nq, int64_t max_n)
 {
-    const int64_t n_chunks = (max_n + kChunk - 1) / kChunk;
+    int64_t n_chunks = (max_n + kChunk - 1) / kChunk;
+    if (n_chunks < kClusterCtas) n_chunks = kClusterCtas;      // the cluster path's per-CTA counts
     size_t s = align_up((size_t)3 * nq * kBins * 4, 256);
     s += align_up((size_t)nq * sizeof(TopkState), 256);
     s += align_up((size_t)nq * n_chunks * 8, 256) * 2;
@@ -346,8 +528,10 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     p.pool_blocks = pool_blocks;
     p.nq = nq;
     p.k = k;
+    p.max_n = max_n;
     p.n_chunks = (int)((max_n + kChunk - 1) / kChunk);
     if (p.n_chunks < 1) p.n_chunks = 1;
+    const int64_t ws_chunks = p.n_chunks < kClusterCtas ? kClusterCtas : p.n_chunks;
     p.idx_out = idx_out;
     p.ld_idx = ld_idx;
     p.cnt_out = cnt_out;
@@ -357,9 +541,18 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     p.state = reinterpret_cast<TopkState *>(w);
     w += align_up((size_t)nq * sizeof(TopkState), 256);
     p.ccount = reinterpret_cast<uint32_t *>(w);
-    w += align_up((size_t)nq * p.n_chunks * 8, 256);
+    w += align_up((size_t)nq * ws_chunks * 8, 256);
     p.coff = reinterpret_cast<uint32_t *>(w);
 
+    if (max_n <= kClusterMax) {
+        const int chunk = (int)(((max_n + kClusterCtas - 1) / kClusterCtas + 3) & ~3);
+        const size_t smem = (size_t)chunk * 4;
+        cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kClChunkMax * 4));
+        topk_cluster_kernel<<<dim3(kClusterCtas, nq), kClThreads, smem, st>>>(p);
+        note_launch();
+        return cudaGetLastError();
+    }
     const dim3 grid2(p.n_chunks, nq);
     topk_init_kernel<<<nq, 256, 0, st>>>(p);
     note_launch();
