@@ -28,6 +28,7 @@ namespace csa2 {
 
 constexpr int kIdxThreads = 192;
 constexpr int kTile = 128;
+constexpr int kEpiBatch = 4;          // tiles the epilogue takes per pass (decode)
 
 struct IndexParams {
     const float *kscale;
@@ -140,8 +141,10 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
 }
 
 // ---------------------------------------------------------------- main kernel
+// Position in this CTA's unit range: group g, tile t of it, and gt = tiles of
+// group g (kept in a register: the global copy is read only on a group change).
 struct UnitIter {
-    int g, t;
+    int g, t, gt;
     int64_t u, u1;
 };
 
@@ -149,7 +152,11 @@ __device__ __forceinline__ void unit_next(UnitIter &it, const int32_t *gtiles, i
 {
     ++it.u;
     ++it.t;
-    while (it.g < n_groups && it.t >= gtiles[it.g]) { ++it.g; it.t = 0; }
+    while (it.g < n_groups && it.t >= it.gt) {
+        ++it.g;
+        it.t = 0;
+        it.gt = it.g < n_groups ? gtiles[it.g] : 0;
+    }
 }
 
 template <int D_IDX>
@@ -233,6 +240,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     UnitIter it0;
     it0.g = sI[1];
     it0.t = sI[6];
+    it0.gt = it0.g < p.n_groups ? p.gtiles[it0.g] : 0;
     it0.u = reinterpret_cast<int64_t *>(sI + 2)[0];
     it0.u1 = reinterpret_cast<int64_t *>(sI + 2)[1];
 
@@ -244,13 +252,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             uint32_t phase = 0;
             int prev_g = -1, bidx = 1;
             uint32_t buse[2] = {0, 0};
-            uint32_t armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // stages <= 8
+            int64_t n_issued = 0;
+            int b = 0;
+            int64_t base = 0, room = 0;
             while (it.u < it.u1) {
                 const int g = it.g, t = it.t;
                 const int q0 = g * p.group;
-                const int b = p.q_seq[q0];
-                const int64_t base = p.seq_base[b];
                 if (g != prev_g) {
+                    b = p.q_seq[q0];
+                    base = p.seq_base[b];
+                    room = p.seq_base[b + 1] - base;
                     bidx ^= 1;
                     if (!mbar_wait(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)) break;
                     ++buse[bidx];
@@ -275,7 +286,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                     const int nblk = (pn + 7) / 8;
                     const int bb0 = t * (kTile / 8);
                     const int nb = min(kTile / 8, nblk - bb0);
-                    const int64_t room = p.seq_base[b + 1] - base;
                     int nvalid = 0;
                     for (int i = 0; i < nb; ++i) {
                         const int blk = p.pool_blk[(int64_t)q * p.pool_blocks + bb0 + i];
@@ -291,16 +301,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                         bulk_load(dstK + i * 8, p.kscale + r, 32u, &full[stage]);
                     }
                 }
-                ++armed[stage];
+                ++n_issued;
                 if (++stage == stages) { stage = 0; phase ^= 1u; }
                 unit_next(it, p.gtiles, p.n_groups);
             }
             if (it.u < it.u1) { *abort_flag = 1; count_event(p.counters, CSA2_CNT_TIMEOUT); }
             // no copy of ours may still be landing when the CTA exits: wait (bounded)
-            // for the last arming of every stage and query buffer
+            // for the last arming of every stage (issue i used stage i % stages, its
+            // (i / stages)-th arming) and of every query buffer
             volatile int no_abort = 0;
-            for (int s = 0; s < stages; ++s)
-                if (armed[s]) mbar_wait(&full[s], (armed[s] - 1u) & 1u, &no_abort);
+            for (int s = 0; s < stages; ++s) {
+                if (n_issued <= s) continue;
+                const int64_t last = s + (n_issued - 1 - s) / stages * stages;
+                mbar_wait(&full[s], (uint32_t)((last / stages) & 1), &no_abort);
+            }
             for (int i = 0; i < 2; ++i)
                 if (buse[i]) mbar_wait(&bfull[i], (buse[i] - 1u) & 1u, &no_abort);
         }
@@ -362,6 +376,65 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 ntq = p.nt[q0];
                 prev_g = g;
             }
+            if (p.group == 1) {
+                // up to kEpiBatch consecutive tiles of this query per pass: all their
+                // TMEM loads are in flight together, one wait, one release each
+                int nb = 0, bt[kEpiBatch], bs[kEpiBatch], ba[kEpiBatch];
+                bool ok = true;
+                {
+                    UnitIter pk = it;
+                    while (nb < kEpiBatch && pk.u < pk.u1 && pk.g == g) {
+                        ok = ok && mbar_wait(&tfull[acc], aphase, abort_flag);
+                        // the stage's TMA data (key scales) is complete: observe it directly
+                        ok = ok && mbar_wait(&full[stage], sphase, abort_flag);
+                        bt[nb] = pk.t; bs[nb] = stage; ba[nb] = acc; ++nb;
+                        if (++stage == stages) { stage = 0; sphase ^= 1u; }
+                        if (++acc == nacc) { acc = 0; aphase ^= 1u; }
+                        unit_next(pk, p.gtiles, p.n_groups);
+                    }
+                    it = pk;
+                }
+                // warp-uniform: the TMEM loads below are .sync.aligned
+                if (!__all_sync(0xffffffffu, ok)) {
+                    *abort_flag = 1;
+                    if (lane == 0) count_event(p.counters, CSA2_CNT_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                float v[kEpiBatch][16];
+#pragma unroll
+                for (int b = 0; b < kEpiBatch; ++b)
+                    if (b < nb)
+                        tmem_ld16(tmem_base + ((quarter * 32u) << 16) + (uint32_t)ba[b] * ncols_acc, v[b]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    for (int b = 0; b < nb; ++b) mbar_arrive(&tempty[ba[b]]);
+#pragma unroll
+                for (int b = 0; b < kEpiBatch; ++b) {
+                    if (b >= nb) break;
+                    const int64_t j = (int64_t)bt[b] * kTile + row;
+                    float sc = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) sc = fmaf(wsr[h], fmaxf(v[b][h], 0.f), sc);
+                    sc *= sK[bs[b] * kTile + row];
+                    const bool valid = j < ntq;
+                    if (valid) p.scores[(int64_t)q0 * p.ld + j] = sc;
+                    if (p.blockmax != nullptr) {
+                        float bm = valid ? sc : -INFINITY;
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                        if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q0 * p.ld_bm + (j >> 3)] = bm;
+                    }
+                }
+                // this warp is done with the stages' key scales: its share of their release
+                __syncwarp();
+                if (lane == 0)
+                    for (int b = 0; b < nb; ++b) mbar_arrive(&empty[bs[b]]);
+                continue;
+            }
             // warp-uniform waits: the TMEM loads below are .sync.aligned
             bool ok = mbar_wait(&tfull[acc], aphase, abort_flag);
             // the stage's TMA data (key scales) is complete: observe it directly
@@ -376,27 +449,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             const int64_t j = (int64_t)t * kTile + row;
             const float sk = sK[stage * kTile + row];
             const uint32_t tbase = tmem_base + ((quarter * 32u) << 16) + (uint32_t)acc * ncols_acc;
-            if (p.group == 1) {
-                float v[16];
-                tmem_ld16(tbase, v);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
-                float s = 0.f;
-#pragma unroll
-                for (int h = 0; h < 16; ++h) s = fmaf(wsr[h], fmaxf(v[h], 0.f), s);
-                s *= sk;
-                const bool valid = j < ntq;
-                if (valid) p.scores[(int64_t)q0 * p.ld + j] = s;
-                if (p.blockmax != nullptr) {
-                    float bm = valid ? s : -INFINITY;
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-                    if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q0 * p.ld_bm + (j >> 3)] = bm;
-                }
-            } else {
+            {
                 // group of queries: h_idx columns per query, 16 columns per load
                 const int hq = p.h_idx;
                 for (int c0 = 0; c0 < p.group * hq; c0 += 16) {
@@ -522,8 +575,8 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
     index_prep_kernel<<<p.n_groups, 256, 0, st>>>(p);
     note_launch();
 
-    const int stages = (p.n_pad <= 64) ? 8 : 6;
-    const int nacc = (p.n_pad <= 64) ? 4 : 2;
+    const int stages = (p.n_pad <= 64) ? (c.d_idx == 128 ? 12 : 16) : 6;
+    const int nacc = (p.n_pad <= 64) ? 8 : 2;
     const size_t smem = index_smem_bytes(c.d_idx, p.n_pad, stages, nacc);
     const int grid = device_sm_count();
     if (c.d_idx == 128) {
@@ -540,3 +593,4 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
 }
 
 }  // namespace csa2
+
