@@ -64,12 +64,11 @@ cudaError_t make_tmap_rows_u8(CUtensorMap *map, const void *base, int64_t rows, 
 }
 
 // ---------------------------------------------------------------- attention plan
-// Rows of a query are processed in 128-row tiles; a query's tiles are split
-// over CTAs so that the grid fills the SMs in one wave (one CTA per SM: the
-// kernel uses ~210 KB of shared memory and all 512 TMEM columns).
-void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_split)
+// Rows of a query are processed in 128-row tiles; a query's tiles are divided
+// over `splits` CTAs so that the grid fills the SMs in one wave (one CTA per
+// SM: the kernel uses ~215 KB of shared memory and all 512 TMEM columns).
+int attn_plan(int nq, int k_max, int n_win)
 {
-    (void)H;
     const int rows = k_max + n_win > 0 ? k_max + n_win : 1;
     const int tiles = (rows + 127) / 128;
     const int sms = device_sm_count();
@@ -77,15 +76,12 @@ void attn_plan(int nq, int H, int k_max, int n_win, int *splits, int *rows_per_s
     if (s > tiles) s = tiles;
     if (s > 152) s = 152;                  // the combine kernel holds at most 152 split weights
     if (s < 1) s = 1;
-    const int tps = (tiles + s - 1) / s;
-    *rows_per_split = tps * 128;
-    *splits = (tiles + tps - 1) / tps;
+    return s;
 }
 
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win)
 {
-    int splits, rps;
-    attn_plan(nq, H, k_max, n_win, &splits, &rps);
+    const int splits = attn_plan(nq, k_max, n_win);
     return align_up((size_t)nq * splits * H * CSA2_D * 4, 256) +
            align_up((size_t)nq * splits * H * 2 * 4, 256);
 }
@@ -319,7 +315,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
     p.sm_scale = sm_scale;
     p.out = out;
     p.lse = lse;
-    attn_plan(p.nq, H, k_max, n_win, &p.splits, &p.rows_per_split);
+    p.splits = attn_plan(p.nq, k_max, n_win);
     uint8_t *w = static_cast<uint8_t *>(workspace);
     p.part_o = reinterpret_cast<float *>(w);
     w += align_up((size_t)p.nq * p.splits * H * CSA2_D * 4, 256);

@@ -27,9 +27,18 @@
 // cross-row max reduction runs only when a logit exceeds its head's reference
 // max by more than 8 (always on the first tile); row sums are kept per thread
 // and reduced once.  Partials (O unnormalised [channel][head], reference max,
-// sum) go to the workspace; the combine kernel merges the splits.
+// sum) are merged over the splits of a query in one of two ways.  Up to 8
+// splits form a thread-block cluster: each CTA stages its O^T in its own
+// shared memory, and after a cluster barrier every CTA sums, for its share of
+// the channels, the staged blocks of all splits read through distributed
+// shared memory, weighted by 2^(m_s - M) / L, and writes the output.  More
+// splits write partials to the workspace for the combine kernel.
+#include <cooperative_groups.h>
+
 #include "csa2_device.cuh"
 #include "csa2_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa2 {
 
@@ -257,6 +266,23 @@ __device__ __forceinline__ void named_sync_all_workers()
     asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// Cluster merge: a block of the receive area is one 32-channel chunk of one
+// split, [64 heads][32 channels] fp32 (8 KB), so that a warp (lane = channel)
+// writes and reads 128 contiguous bytes per head.
+constexpr int kXBlock = 64 * 32;
+constexpr int kMaxClusterSplits = 8;
+
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+template <bool kCluster>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 {
     const int q = blockIdx.y, split = blockIdx.x;
@@ -274,7 +300,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     float *sAlpha = sM + 64;                  // rescale factor of the current tile
     float *sL = sAlpha + 64;                  // running sum per head
     float *sRedL = sL + 64;                   // [4 quarters][64 heads] tile row sums
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sRedL + 4 * 64);
+    float *sML = sRedL + 4 * 64;              // cluster merge: [split][m | l][64 heads]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sML + kMaxClusterSplits * 2 * 64);
     uint64_t *bar_v = bars, *bar_s = bars + 1, *bar_p = bars + 2, *bar_o = bars + 3;
     uint64_t *bar_done = bars + 4, *bar_q = bars + 5;
     int *sFlag = reinterpret_cast<int *>(bars + 6);   // [0] abort [1] rescale [2] bad [3] need max
@@ -283,9 +310,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 
     const TcRowSet rs = tc_row_set(p, q);
     const int n_rows = rs.cnt + rs.nw;
-    const int r_begin = split * p.rows_per_split;
-    const int r_end = min(n_rows, r_begin + p.rows_per_split);
-    const int n_tiles = (r_end > r_begin) ? (r_end - r_begin + kRows - 1) / kRows : 0;
+    // this query's tiles, ceil(tiles / splits) per split: the last split, which
+    // holds the window rows (the slower tile), gets the remainder
+    const int q_tiles = (n_rows + kRows - 1) / kRows;
+    const int tps = (q_tiles + p.splits - 1) / p.splits;
+    const int t_begin = min(q_tiles, split * tps);
+    const int t_end = min(q_tiles, t_begin + tps);
+    const int r_begin = t_begin * kRows;
+    const int r_end = min(n_rows, t_end * kRows);
+    const int n_tiles = t_end - t_begin;
 
     if (tid == 0) {
         mbar_init(bar_v, kWorkers / 32);
@@ -301,6 +334,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         fence_barrier_init();
     }
     if (tid < 64) { sM[tid] = -INFINITY; sAlpha[tid] = 1.f; sL[tid] = 0.f; }
+    // a CTA's shared memory may be written by its cluster peers only once it runs:
+    // arrive now, wait before the first remote store (the merge at the end)
+    if constexpr (kCluster) cluster_arrive();
     if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
 
     // ---- Q: one bulk copy of the raw bf16 block [H][512] into the (still free)
@@ -315,81 +351,121 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int wt = tid - 32;                          // worker index 0..255
     const uint32_t quarter = (uint32_t)(warp & 3);    // TMEM lanes 32 quarter ..
     const int row = (int)(quarter * 32 + lane);       // tile row == TMEM lane of this thread
-    const int half = (warp - 1) >> 2;                 // channels 256 half .., heads 32 half ..
-    uint4 rc[8], rsc;                                 // half an FP4 row: 128 B codes + 16 B scales
-    int kind = 0;                                     // 0 empty, 1 fp4, 2 window
-    int64_t wrow = 0;
-    int next_j = -1;
-    auto entry_of = [&](int tile) -> int {
-        const int g = r_begin + tile * kRows + row;
-        return (g < r_end && g < rs.cnt) ? p.idx[(int64_t)q * p.ld_idx + g] : -1;
+    const int half = (warp - 1) >> 2;                 // heads 32 half .. of its softmax
+
+    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15, two rows per
+    // load instruction: lanes 0-15 take row 2t, lanes 16-31 row 2t + 1 of pair t, and
+    // lane sub = lane & 15 holds channels 32 sub .. 32 sub + 31 of that row (16 code
+    // bytes, 2 scale bytes).  A warp load then touches 4 lines, not 32 (one per
+    // row), which keeps the load/store unit free for the shared-memory traffic of
+    // the softmax.  The next tile's codes are loaded while this tile is in flight.
+    const int wg = warp - 1;
+    const int sub = lane & 15;
+    uint4 gc[8];                  // codes of pair t
+    uint32_t gsc[8];              // the two scale bytes of those channels
+    uint32_t gkind = 0;           // bit t: FP4 row with data; bit 8 + t: window row
+    int gj = -1;                  // entry of row 16 wg + sub of the tile gathered next
+    auto tile_row = [&](int tile, int r) { return r_begin + tile * kRows + r; };
+    // entry of tile row r (-1 for window rows and rows past the end)
+    auto entry = [&](int tile, int r) {
+        const int g = tile_row(tile, r);
+        return (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
     };
-    auto fetch = [&](int tile, int j) {
-        const int g = r_begin + tile * kRows + row;
-        kind = 0;
-        if (g < r_end) {
-            if (g < rs.cnt) {
-                if (j >= 0 && j < rs.nt) {
-                    kind = 1;
-                    const int64_t r = rs.base + j;
-                    const uint4 *c4 = reinterpret_cast<const uint4 *>(
-                        p.codes + r * CSA2_CODE_BYTES + half * (CSA2_CODE_BYTES / 2));
+    auto gather = [&](int tile) {
+        gkind = 0;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) rc[k] = __ldg(c4 + k);
-                    rsc = __ldg(reinterpret_cast<const uint4 *>(p.scales + r * CSA2_SCALE_BYTES) + half);
+        for (int t = 0; t < 8; ++t) {
+            const int slot = 2 * t + (lane >> 4);
+            const int g = tile_row(tile, 16 * wg + slot);
+            const int j = __shfl_sync(0xffffffffu, gj, slot);
+            if (g < r_end && g < rs.cnt) {
+                if (j >= 0 && j < rs.nt) {
+                    const int64_t r = rs.base + j;
+                    gc[t] = __ldg(reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES) + sub);
+                    gsc[t] = __ldg(reinterpret_cast<const uint16_t *>(p.scales + r * CSA2_SCALE_BYTES) + sub);
+                    gkind |= 1u << t;
                 } else {
                     sFlag[2] = 1;
                 }
+            } else if (g < r_end) {
+                gkind |= 1u << (8 + t);
+            }
+        }
+    };
+    // Stores of one lane: its 32 channels are 4 16-byte chunks 4 (sub & 1) + m of
+    // atom column sub >> 1.  Store j writes chunk m = (j + atom) & 3, so that the
+    // 32 lanes of one store spread over all eight 16-byte bank groups.
+    auto put4 = [&](int r, const uint4 (&v)[4]) {
+        const int a = sub >> 1, ph = sub & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = (j + a) & 3;
+            const uint4 x = (m & 2) ? ((m & 1) ? v[3] : v[2]) : ((m & 1) ? v[1] : v[0]);
+            *reinterpret_cast<uint4 *>(sV + a * kVAtom + sw128((uint32_t)r, (uint32_t)(4 * ph + m))) = x;
+        }
+    };
+    auto store_v = [&](int tile) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int r = 16 * wg + 2 * t + (lane >> 4);
+            uint4 v[4];
+            if (gkind & (1u << t)) {
+                const uint32_t p0 = scale_pair(gsc[t] & 0xFFu), p1 = scale_pair((gsc[t] >> 8) & 0xFFu);
+                v[0] = fp4x8_to_f16(gc[t].x, p0);
+                v[1] = fp4x8_to_f16(gc[t].y, p0);
+                v[2] = fp4x8_to_f16(gc[t].z, p1);
+                v[3] = fp4x8_to_f16(gc[t].w, p1);
+            } else if (gkind & (1u << (8 + t))) {
+                const int64_t pos = rs.lo + (tile_row(tile, r) - rs.cnt);
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 4 * sub;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 raw = __ldg(src + k);
+                    v[k] = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
+                                      bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
+                }
             } else {
-                kind = 2;
-                const int64_t pos = rs.lo + (g - rs.cnt);
-                wrow = ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D + half * (CSA2_D / 2);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
             }
+            put4(r, v);
         }
     };
-    // dequantise (or copy) this thread's half row into the f16 V tile
-    auto store_v = [&]() {
-        if (kind == 1) {
-            const uint32_t sw[4] = {rsc.x, rsc.y, rsc.z, rsc.w};   // 16 scale bytes
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {                // atom column 4 half + a
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {            // 8 channels = 4 code bytes
-                    const int word = a * 8 + c;
-                    const uint4 &u = rc[word >> 2];
-                    const uint32_t w = (word & 3) == 0 ? u.x : (word & 3) == 1 ? u.y
-                                     : (word & 3) == 2 ? u.z : u.w;
-                    const int grp = (64 * a + 8 * c) >> 4;       // scale group within the half
-                    const uint32_t sb = (sw[grp >> 2] >> (8 * (grp & 3))) & 0xFFu;
-                    *reinterpret_cast<uint4 *>(sV + (4 * half + a) * kVAtom + sw128(row, c)) =
-                        fp4x8_to_f16(w, scale_pair(sb));
-                }
-            }
-        } else if (kind == 2) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.win + wrow);
-#pragma unroll 1
-            for (int b16 = 0; b16 < 2; ++b16) {          // 2 batches of 16 loads in flight
-                uint4 raw[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) raw[k] = __ldg(src + 16 * b16 + k);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int kk = 16 * b16 + k;         // 16-byte chunk of the half row
-                    *reinterpret_cast<uint4 *>(sV + (4 * half + (kk >> 3)) * kVAtom + sw128(row, kk & 7)) =
-                        make_uint4(bf16x2_to_f16x2(raw[k].x), bf16x2_to_f16x2(raw[k].y),
-                                   bf16x2_to_f16x2(raw[k].z), bf16x2_to_f16x2(raw[k].w));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                *reinterpret_cast<uint4 *>(sV + (4 * half + (k >> 3)) * kVAtom + sw128(row, k & 7)) =
-                    make_uint4(0, 0, 0, 0);
-        }
-    };
+    int my_j = -1;                // entry of this thread's softmax row in the current tile
     if (warp > 0 && n_tiles > 0) {
-        fetch(0, entry_of(0));
-        if (n_tiles > 1) next_j = entry_of(1);
+        gj = lane < 16 ? entry(0, 16 * wg + sub) : -1;
+        my_j = entry(0, row);
+        gather(0);
+        // Every CTA gathers in step with the others, so each tile's gather is a burst
+        // of random rows from HBM that stalls the issuing warps.  Asking L2 for all
+        // rows of the later tiles now (bulk prefetches, nothing waits for them) turns
+        // those gathers into L2 hits.
+        // (the entries are read four at a time so that their loads overlap)
+        for (int g0 = r_begin + kRows + wt; g0 < r_end; g0 += 4 * kWorkers) {
+            int jj[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = g0 + u * kWorkers;
+                jj[u] = (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = g0 + u * kWorkers;
+                if (g >= r_end) break;
+                if (g < rs.cnt) {
+                    if (jj[u] >= 0 && jj[u] < rs.nt) {
+                        const int64_t r = rs.base + jj[u];
+                        bulk_prefetch_l2(p.codes + r * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+                        bulk_prefetch_l2(p.scales + r * CSA2_SCALE_BYTES, CSA2_SCALE_BYTES);
+                    }
+                } else {
+                    const int64_t pos = rs.lo + (g - rs.cnt);
+                    bulk_prefetch_l2(p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D, CSA2_D * 2);
+                }
+            }
+        }
+        if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + sub) : -1;
     }
     {
         volatile int no_abort = 0;
@@ -462,14 +538,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 if (!ok) break;
                 tc_fence_after();
             }
-            const bool valid = kind != 0;
-            store_v();
+            const int g_row = tile_row(i, row);
+            const bool valid = g_row < r_end && (g_row >= rs.cnt || (my_j >= 0 && my_j < rs.nt));
+            store_v(i);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_v);
+            int my_j_next = -1;
             if (i + 1 < n_tiles) {
-                fetch(i + 1, next_j);
-                if (i + 2 < n_tiles) next_j = entry_of(i + 2);
+                gather(i + 1);
+                if (i + 2 < n_tiles) gj = lane < 16 ? entry(i + 2, 16 * wg + sub) : -1;
+                my_j_next = entry(i + 1, row);
             }
 
             // ---- softmax of this row, heads h0 .. h0+31
@@ -570,46 +649,129 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             named_sync_all_workers();
             if (wt < 64)
                 sL[wt] += (sRedL[wt] + sRedL[64 + wt]) + (sRedL[128 + wt] + sRedL[192 + wt]);
+            my_j = my_j_next;
         }
         if (!ok) *abort_flag = 1;
         named_sync_all_workers();
 
-        // ---- epilogue: O^T (unnormalised) -> partials [split][channel][head]
+        // ---- epilogue: O^T (unnormalised) of this split
         if (ok && n_tiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
             tc_fence_after();
         }
-        const int64_t pbase = (int64_t)q * p.splits + split;
-        if (ok) {
-            float *po = p.part_o + pbase * CSA2_D * H;
+        if (!ok) *abort_flag = 1;
+        if constexpr (!kCluster) {
+            const int64_t pbase = (int64_t)q * p.splits + split;
+            if (ok) {
+                float *po = p.part_o + pbase * CSA2_D * H;
+#pragma unroll 1
+                for (int mb = 0; mb < 4; ++mb) {
+                    float o[32];
+                    if (n_tiles > 0) {
+                        tmem_ld32(tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16), o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) o[h] = 0.f;
+                    }
+                    float *dst = po + (int64_t)(128 * mb + row) * H + h0;
+                    if (h0 + 32 <= H) {
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4)
+                            reinterpret_cast<float4 *>(dst)[h4] =
+                                make_float4(o[4 * h4], o[4 * h4 + 1], o[4 * h4 + 2], o[4 * h4 + 3]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 32; ++h)
+                            if (h0 + h < H) dst[h] = o[h];
+                    }
+                }
+                if (wt < H) {
+                    p.part_ml[(pbase * H + wt) * 2] = (n_tiles > 0) ? sM[wt] : -INFINITY;
+                    p.part_ml[(pbase * H + wt) * 2 + 1] = (n_tiles > 0) ? sL[wt] : 0.f;
+                }
+            }
+        }
+        if (wt == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+    }
+
+    if constexpr (kCluster) {
+        // ---- merge of the cluster's splits.  Every thread of every CTA reaches
+        // each cluster barrier exactly once, whatever happened above.  32-channel
+        // chunk c belongs to CTA c % S; each CTA scales its O^T block by
+        // 2^(m_s - M) / L and stores it into the owner's receive area, block
+        // (c / S) S + sender, which the owner then sums locally.
+        cg::cluster_group cluster = cg::this_cluster();
+        const int S = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+        float *sFac = reinterpret_cast<float *>(sP);          // [split][head]
+        float *sX = reinterpret_cast<float *>(sV);            // receive area (V and Q tiles)
+        cluster_wait();              // (arrived at the start) every CTA of the cluster runs
+        // this split's reference max and sum go to every CTA's own table (a peer's
+        // V, Q and P tiles may still be in use)
+        if (tid < 64) {
+            const bool any = !*abort_flag && n_tiles > 0;
+            const float m = any ? sM[tid] : -INFINITY, l = any ? sL[tid] : 0.f;
+            for (int s = 0; s < S; ++s) {
+                float *t = cluster.map_shared_rank(sML, s);
+                t[rank * 128 + tid] = m;
+                t[rank * 128 + 64 + tid] = l;
+            }
+        }
+        cluster.sync();              // every split has finished its tiles; all m, l delivered
+        if (tid < 64) {
+            float M = -INFINITY;
+            for (int s = 0; s < S; ++s) M = fmaxf(M, sML[s * 128 + tid]);
+            float L = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float ms = sML[s * 128 + tid];
+                const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
+                sFac[s * 64 + tid] = w;
+                L = fmaf(sML[s * 128 + 64 + tid], w, L);
+            }
+            const float inv = (L > 0.f) ? 1.f / L : 0.f;
+            for (int s = 0; s < S; ++s) sFac[s * 64 + tid] *= inv;
+            if (p.lse != nullptr && rank == 0 && tid < H)
+                p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        }
+        __syncthreads();
+        if (warp > 0) {
+            const int h0 = 32 * half;
+            const bool any = !*abort_flag && n_tiles > 0;
+            float f[32];
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 a4 = reinterpret_cast<const float4 *>(sFac + rank * 64 + h0)[h4];
+                f[4 * h4] = a4.x; f[4 * h4 + 1] = a4.y; f[4 * h4 + 2] = a4.z; f[4 * h4 + 3] = a4.w;
+            }
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
                 float o[32];
-                if (n_tiles > 0) {
+                if (any) {
                     tmem_ld32(tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16), o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int h = 0; h < 32; ++h) o[h] = 0.f;
                 }
-                float *dst = po + (int64_t)(128 * mb + row) * H + h0;
-                if (h0 + 32 <= H) {
+                const int c = 4 * mb + (int)quarter;
+                float *dst = cluster.map_shared_rank(sX, c % S) +
+                             ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
 #pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4)
-                        reinterpret_cast<float4 *>(dst)[h4] =
-                            make_float4(o[4 * h4], o[4 * h4 + 1], o[4 * h4 + 2], o[4 * h4 + 3]);
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 32; ++h)
-                        if (h0 + h < H) dst[h] = o[h];
-                }
-            }
-            if (wt < H) {
-                p.part_ml[(pbase * H + wt) * 2] = (n_tiles > 0) ? sM[wt] : -INFINITY;
-                p.part_ml[(pbase * H + wt) * 2 + 1] = (n_tiles > 0) ? sL[wt] : 0.f;
+                for (int h = 0; h < 32; ++h) dst[h * 32] = o[h] * f[h];
             }
         }
-        if (wt == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+        cluster.sync();              // every block has arrived at its owner
+        // chunks rank, rank + S, ...: lane = channel, one head per warp and item
+        const int n_own = (16 - rank + S - 1) / S;
+        for (int it = warp; it < n_own * H; it += kTcThreads / 32) {
+            const int k = it / H, h = it % H, c = rank + k * S;
+            const float *src = sX + k * S * kXBlock + h * 32 + lane;
+            float v[kMaxClusterSplits];
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) v[s] = (s < S) ? src[s * kXBlock] : 0.f;
+            p.out[((int64_t)q * H + h) * CSA2_D + 32 * c + lane] =
+                ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+        }
     }
 
     tc_fence_before();
@@ -671,11 +833,35 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p)
     }
 }
 
+bool attn_uses_cluster(int splits) { return splits <= kMaxClusterSplits; }
+
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
-    const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 + 6 * 8 + 64;
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attn_tc_kernel<<<dim3(p.splits, p.nq), kTcThreads, smem, st>>>(p);
+    // receive area: ceil(16 / S) chunk slots x S senders blocks, largest at S = 7 (21)
+    static_assert(21 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
+    static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
+    const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
+                        kMaxClusterSplits * 2 * 64 * 4 + 6 * 8 + 64;
+    if (attn_uses_cluster(p.splits)) {
+        cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.splits, p.nq);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)p.splits;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, p);
+        note_launch(1);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attn_tc_kernel<false><<<dim3(p.splits, p.nq), kTcThreads, smem, st>>>(p);
     attn_combine_kernel<<<dim3(CSA2_D / 32, p.nq), 256, 0, st>>>(p);
     note_launch(2);
     return cudaGetLastError();
