@@ -133,9 +133,9 @@ csa2_status csa2_quantize_append(const csa2_cache *cache, const float *C, const 
 
 /* ---- 2. Full-mode indexer -------------------------------------------------
  * scores[i][j] = sum_h w[i][h] * ReLU(q_h . k_j) for the visible entries
- * j < N_i = floor((q_pos[i]+1)/m) of query i ([Notes] section 2, Full mode
- * "scores the entire visible context"), with q_h FP8-quantised per head by the
- * library.  Entries j >= N_i are not written.  If blockmax is not NULL it also
+ * j < N_i = floor((q_pos[i]+1)/m) of query i ([Notes] section 2: a Full
+ * layer scores every entry the query can see), with q_h FP8-quantised per head
+ * by the library.  Entries j >= N_i are not written.  If blockmax is not NULL it also
  * receives, for each aligned 8-entry block b holding a visible entry, the max
  * score over the block's visible entries ([Notes] section 3, step 1).
  * n_valid[i] (nullable) receives N_i.

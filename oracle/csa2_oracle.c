@@ -48,7 +48,7 @@
 /* ------------------------------------------------------------------------ */
 
 /* E2M1: sign bit, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is
- * subnormal.  [Notes] section 4: "E2M1 elements". */
+ * subnormal.  [Notes] section 4 (main-KV elements are E2M1). */
 double or_e2m1_value(int nib)
 {
     int s = (nib >> 3) & 1, e = (nib >> 1) & 3, mt = nib & 1;

@@ -19,7 +19,7 @@ def golden(name):
 
 def read_constants():
     out = {}
-    with open(golden("paper_constants.txt")) as f:
+    with open(golden("page_constants.txt")) as f:
         for line in f:
             line = line.split("#", 1)[0].strip()
             if line:

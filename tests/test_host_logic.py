@@ -10,15 +10,15 @@ import torch.multiprocessing as mp
 from conftest import ROOT, read_constants
 from sparse_attention_decode_step_gb300 import schedule as S
 
-PAPER = read_constants()
+PAGES = read_constants()
 
 
 def test_indexer_count_matches_pages():
     # [Notes] section 2: 3 indexers in the encoder, 5 in the decoder, 40 layers
     enc, dec = S.encoder_schedule(), S.decoder_schedule()
-    assert len(enc) == 20 and len(dec) == 20 and len(enc) + len(dec) == PAPER["layers_total"]
-    assert len(S.indexer_layers(enc)) == PAPER["indexers_encoder"]
-    assert len(S.indexer_layers(dec)) == PAPER["indexers_decoder"]
+    assert len(enc) == 20 and len(dec) == 20 and len(enc) + len(dec) == PAGES["layers_total"]
+    assert len(S.indexer_layers(enc)) == PAGES["indexers_encoder"]
+    assert len(S.indexer_layers(dec)) == PAGES["indexers_decoder"]
 
 
 def test_decoder_blocks_and_reuse_sources():
@@ -50,7 +50,7 @@ def test_entries_per_token_and_kv_accounting():
     # at 288 + 64 + 4 B per entry that is the pages' 890 B/token
     ept = S.entries_per_token()
     assert ept == 2.5
-    assert ept * (288 + 64 + 4) == PAPER["global_kv_bytes_per_token"]
+    assert ept * (288 + 64 + 4) == PAGES["global_kv_bytes_per_token"]
 
 
 def _replica_worker(rank, world, port, q):

@@ -15,7 +15,7 @@ import torch
 import oracle as O
 from conftest import golden, read_constants
 
-PAPER = read_constants()
+PAGES = read_constants()
 
 
 # --------------------------------------------------------------- formats
@@ -45,7 +45,7 @@ def test_e4m3_decode_matches_library():
 def test_e4m3_constants():
     pos = [O.e4m3_value(b) for b in range(1, 0x7F)]
     assert len(pos) == 126 and all(np.diff(pos) > 0)
-    assert max(pos) == PAPER["e4m3_max"]            # 448
+    assert max(pos) == PAGES["e4m3_max"]            # 448
     assert min(pos) == 2.0 ** -9
     assert O.e4m3_value(0x38) == 1.0
 
@@ -53,7 +53,7 @@ def test_e4m3_constants():
 def test_fp4_range_is_paper_figure():
     # [Notes] section 4: representable range 448 x 6 = 2688
     top = max(O.e2m1_value(c) for c in range(16)) * max(O.e4m3_value(b) for b in range(0x7F))
-    assert top == PAPER["fp4_range"] == PAPER["e4m3_max"] * PAPER["e2m1_max"]
+    assert top == PAGES["fp4_range"] == PAGES["e4m3_max"] * PAGES["e2m1_max"]
 
 
 def test_e4m3_nearest_matches_library_rne():
@@ -178,7 +178,7 @@ def test_fp4_roundtrip_of_representable_values():
 def test_fp4_granularity_and_bytes_per_entry():
     codes, scales, _ = O.fp4_encode_entry(np.ones(512))
     assert codes.nbytes == 256 and scales.nbytes == 32
-    assert scales.nbytes == PAPER["latent_width"] / PAPER["scale_group"]
+    assert scales.nbytes == PAGES["latent_width"] / PAGES["scale_group"]
     assert (codes.nbytes + scales.nbytes) * 8 / 512 == 4.5
 
 
@@ -187,7 +187,7 @@ def test_norm_bound_never_saturates():
     # max |v_i| <= sqrt(512) ~ 22.6; with range 2688 no group saturates and the
     # scale never exceeds the smallest E4M3 >= 22.63 / 6, which is 4.0.
     bound = math.sqrt(512)
-    assert abs(bound - PAPER["latent_bound"]) < 0.05
+    assert abs(bound - PAGES["latent_bound"]) < 0.05
     rng = np.random.default_rng(9)
     cases = []
     for i in range(0, 512, 37):
@@ -344,9 +344,9 @@ def test_pool_size_at_1m_is_paper_figure():
     # [Notes] section 3: 2,048 x 8 = 16,384 positions; 1.6% of a 1M context
     n = 1 << 20
     sc = np.random.default_rng(47).normal(size=n)
-    blk, pn = O.pool(sc, int(PAPER["pool_blocks"]))
-    assert len(blk) == PAPER["pool_blocks"] and pn == PAPER["pool_positions"]
-    assert round(100 * pn / n, 1) == PAPER["pool_fraction_1m_pct"]
+    blk, pn = O.pool(sc, int(PAGES["pool_blocks"]))
+    assert len(blk) == PAGES["pool_blocks"] and pn == PAGES["pool_positions"]
+    assert round(100 * pn / n, 1) == PAGES["pool_fraction_1m_pct"]
     assert np.all(np.diff(blk) > 0)
     bm = O.blockmax(sc)
     assert np.array_equal(blk, np.sort(np.lexsort((np.arange(len(bm)), -bm))[:2048]))
@@ -492,4 +492,4 @@ def test_kv_bytes_per_token_accounting():
     codes, scales, _ = O.fp4_encode_entry(np.ones(512))
     entries_per_token = 3 * (1 / 2) + 1 * 1
     per_entry = codes.nbytes + scales.nbytes + 64 + 4
-    assert entries_per_token * per_entry == PAPER["global_kv_bytes_per_token"]
+    assert entries_per_token * per_entry == PAGES["global_kv_bytes_per_token"]
