@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(256) append_kernel(csa2_cache cache, const flo
                                                     const float *__restrict__ key, int n_tok,
                                                     int n_ent, uint32_t *counters)
 {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= (int64_t)cache.batch * n_ent) return;
@@ -155,6 +157,8 @@ __global__ void __launch_bounds__(256) append_kernel(csa2_cache cache, const flo
 // as append_kernel, so refused sequences stay unchanged).
 __global__ void append_commit_kernel(csa2_cache cache, int n_ent)
 {
+    pdl_wait();
+    pdl_trigger();
     for (int b = threadIdx.x; b < cache.batch; b += blockDim.x) {
         const int64_t room = cache.seq_base[b + 1] - cache.seq_base[b];
         const int64_t len = cache.seq_len[b];
@@ -168,10 +172,11 @@ cudaError_t launch_append(const csa2_cache &c, const float *C, const float *Z, c
     const int n_ent = n_tok / c.m;
     const int64_t warps = (int64_t)c.batch * n_ent;
     const int64_t blocks = (warps * 32 + 255) / 256;
-    append_kernel<<<(unsigned)blocks, 256, 0, st>>>(c, C, Z, key, n_tok, n_ent, counters);
-    note_launch();
-    append_commit_kernel<<<1, 256, 0, st>>>(c, n_ent);
-    note_launch();
+    cudaError_t e = launch_k(append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 0, c, C, Z,
+                             key, n_tok, n_ent, counters);
+    if (e != cudaSuccess) return e;
+    e = launch_k(append_commit_kernel, dim3(1), dim3(256), 0, st, 0, c, n_ent);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -285,6 +285,8 @@ __device__ __forceinline__ void cluster_wait()
 template <bool kCluster>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.y, split = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -790,6 +792,8 @@ constexpr int kCombineMaxSplits = 152;   // static shared memory stays under 48 
 
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.y, c0 = blockIdx.x * 32;
     const int H = p.H, tid = threadIdx.x, S = p.splits;
     __shared__ float sW[kCombineMaxSplits][64];   // weight of split s for head h
@@ -844,26 +848,16 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
                         kMaxClusterSplits * 2 * 64 * 4 + 6 * 8 + 64;
     if (attn_uses_cluster(p.splits)) {
         cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(p.splits, p.nq);
-        cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = (unsigned)p.splits;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, p);
-        note_launch(1);
+        const cudaError_t e = launch_k(attn_tc_kernel<true>, dim3(p.splits, p.nq), dim3(kTcThreads),
+                                       smem, st, (unsigned)p.splits, p);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attn_tc_kernel<false><<<dim3(p.splits, p.nq), kTcThreads, smem, st>>>(p);
-    attn_combine_kernel<<<dim3(CSA2_D / 32, p.nq), 256, 0, st>>>(p);
-    note_launch(2);
+    cudaError_t e = launch_k(attn_tc_kernel<false>, dim3(p.splits, p.nq), dim3(kTcThreads), smem, st,
+                             0, p);
+    if (e != cudaSuccess) return e;
+    e = launch_k(attn_combine_kernel, dim3(CSA2_D / 32, p.nq), dim3(256), 0, st, 0, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

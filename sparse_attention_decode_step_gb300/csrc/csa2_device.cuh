@@ -120,6 +120,24 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel of the stream is finishing; it
+// calls pdl_wait() before its first access to global memory that an earlier
+// kernel may write (the wait returns once every earlier kernel has completed
+// and its writes are visible), and pdl_trigger() right after, which lets the
+// next kernel be scheduled as this one's CTAs retire.  Only set-up that reads
+// no such memory (barrier init, TMEM allocation, descriptor prefetch) runs
+// before the wait.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Bulk prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned, size % 16 == 0);
 // nothing is written to shared memory and nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes)

@@ -71,6 +71,8 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t r, uint32_t c, uint32_t row
 // image (the smem B operand, pre-swizzled) and w * q scale.
 __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = g * p.group;
@@ -201,6 +203,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         prefetch_tmap(&tmap);
     }
     if (warp == 1) { tmem_alloc(s_tmem, tm_cols); tmem_relinquish(); }
+    // everything above touched no global memory that an earlier kernel writes.
+    // No early trigger here: the top-k clusters that follow would be placed on
+    // the first SMs this kernel frees, several per SM, and run ~1.5x slower
+    // than when they are spread over the whole GPU at once.
+    pdl_wait();
 
     // ---- this CTA's unit range [u0, u1) and its first (group, tile)
     {
@@ -572,8 +579,8 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
                                       pool_blk ? 8 : kTile, c.d_idx == 128 ? 128 : 64);
     if (e != cudaSuccess) return e;
 
-    index_prep_kernel<<<p.n_groups, 256, 0, st>>>(p);
-    note_launch();
+    e = launch_k(index_prep_kernel, dim3(p.n_groups), dim3(256), 0, st, 0, p);
+    if (e != cudaSuccess) return e;
 
     const int stages = (p.n_pad <= 64) ? (c.d_idx == 128 ? 12 : 16) : 6;
     const int nacc = (p.n_pad <= 64) ? 8 : 2;
@@ -582,13 +589,13 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
     if (c.d_idx == 128) {
         auto k = index_main_kernel<128>;
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kIdxThreads, smem, st>>>(tmap, p, stages, nacc);
+        e = launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
     } else {
         auto k = index_main_kernel<64>;
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kIdxThreads, smem, st>>>(tmap, p, stages, nacc);
+        e = launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
     }
-    note_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -55,6 +55,8 @@ __device__ __forceinline__ uint32_t round_bins(int r) { return r == 2 ? 1024u : 
 
 __global__ void topk_init_kernel(TopkParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.x;
     for (int i = threadIdx.x; i < 3 * kBins; i += blockDim.x) {
         const int r = i / kBins, b = i % kBins;
@@ -76,6 +78,8 @@ __global__ void topk_init_kernel(TopkParams p)
 
 __global__ void __launch_bounds__(kTkThreads) topk_hist_kernel(TopkParams p, int r)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.y, c = blockIdx.x;
     const TopkState st = p.state[q];
     if (st.all) return;
@@ -133,6 +137,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *s_warp
 // count(> d) < k_rem <= count(>= d).
 __global__ void __launch_bounds__(kTkThreads) topk_scan_kernel(TopkParams p, int r)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.x;
     TopkState st = p.state[q];
     if (st.all) return;
@@ -199,6 +205,8 @@ __device__ __forceinline__ void load16(const float *row, int64_t i0, int64_t n, 
 
 __global__ void __launch_bounds__(kTkThreads) topk_count_kernel(TopkParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.y, c = blockIdx.x;
     const TopkState st = p.state[q];
     const int64_t i0 = (int64_t)c * kChunk + threadIdx.x * kPerThread;
@@ -228,6 +236,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_count_kernel(TopkParams p)
 
 __global__ void __launch_bounds__(kTkThreads) topk_offsets_kernel(TopkParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.x;
     const TopkState st = p.state[q];
     const int32_t k_eq = st.all ? 0 : st.k_rem;
@@ -262,6 +272,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_offsets_kernel(TopkParams p)
 
 __global__ void __launch_bounds__(kTkThreads) topk_write_kernel(TopkParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.y, c = blockIdx.x;
     const TopkState st = p.state[q];
     const int64_t i0 = (int64_t)c * kChunk + threadIdx.x * kPerThread;
@@ -350,6 +362,8 @@ __device__ __forceinline__ uint32_t scan512(uint32_t v, uint32_t *s_warp, uint32
 __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThreads)
     topk_cluster_kernel(TopkParams p)
 {
+    pdl_wait();
+    pdl_trigger();
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int q = blockIdx.y, rank = (int)cluster.block_rank(), tid = threadIdx.x;
@@ -376,17 +390,29 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
         if (tid == 0) p.cnt_out[q] = all ? n : p.k;
         for (int i = tid; i < 3 * kBins; i += kClThreads) ghist[i] = 0u;
     }
+    for (int i = tid; i < kBins; i += kClThreads) hist[i] = 0u;   // re-cleared by each merge
+    __syncthreads();
 
-    // keys of this CTA's candidates into shared memory (lo is a multiple of 4)
+    // keys of this CTA's candidates into shared memory (lo is a multiple of 4),
+    // with the first round's histogram (top 11 bits) built on the way
     for (int i = tid * 4; i < len; i += kClThreads * 4) {
         if (i + 4 <= len) {
             const float4 f = *reinterpret_cast<const float4 *>(row + lo + i);
-            s_keys[i] = score_key(f.x);
-            s_keys[i + 1] = score_key(f.y);
-            s_keys[i + 2] = score_key(f.z);
-            s_keys[i + 3] = score_key(f.w);
+            const uint32_t k0 = score_key(f.x), k1 = score_key(f.y);
+            const uint32_t k2 = score_key(f.z), k3 = score_key(f.w);
+            *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k0, k1, k2, k3);
+            if (!all) {
+                atomicAdd(&hist[k0 >> 21], 1u);
+                atomicAdd(&hist[k1 >> 21], 1u);
+                atomicAdd(&hist[k2 >> 21], 1u);
+                atomicAdd(&hist[k3 >> 21], 1u);
+            }
         } else {
-            for (int j = i; j < len; ++j) s_keys[j] = score_key(row[lo + j]);
+            for (int j = i; j < len; ++j) {
+                const uint32_t kj = score_key(row[lo + j]);
+                s_keys[j] = kj;
+                if (!all) atomicAdd(&hist[kj >> 21], 1u);
+            }
         }
     }
     cluster.sync();                                              // histograms zeroed, keys loaded
@@ -396,16 +422,18 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
             const int sh = r == 0 ? 21 : (r == 1 ? 10 : 0);
             const int pbits = r == 0 ? 0 : (r == 1 ? 11 : 22);
             const uint32_t nb = r == 2 ? 1024u : 2048u;
-            for (int i = tid; i < kBins; i += kClThreads) hist[i] = 0u;
-            __syncthreads();
-            for (int i = tid; i < len; i += kClThreads) {
-                const uint32_t key = s_keys[i];
-                if (r == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1u)], 1u);
+            if (r > 0) {                                         // round 0 was built with the load
+                for (int i = tid; i < len; i += kClThreads) {
+                    const uint32_t key = s_keys[i];
+                    if ((key >> (32 - pbits)) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1u)], 1u);
+                }
             }
             __syncthreads();
             uint32_t *gh = ghist + r * kBins;
-            for (int i = tid; i < (int)nb; i += kClThreads)
-                if (hist[i]) atomicAdd(gh + i, hist[i]);
+            for (int i = tid; i < (int)nb; i += kClThreads) {
+                const uint32_t h = hist[i];
+                if (h) { atomicAdd(gh + i, h); hist[i] = 0u; }
+            }
             cluster.sync();                                      // the query's histogram is complete
             // digit d with count(> d) < k_rem <= count(>= d); bins from the top, 4 per thread
             uint32_t c[4];
@@ -432,56 +460,64 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
         }
     }
 
-    // ---- ordered compaction: keys > T, then the lowest-position keys == T
+    // ---- ordered compaction: keys > T, then the lowest-position keys == T.
+    // Warp w owns a contiguous segment of this CTA's keys and walks it 32 keys
+    // at a time with ballots: one pass counts, the other writes.  Output slot
+    // of a chosen key = (keys > T before it) + min(keys == T before it, k_rem).
     const uint32_t T = prefix;
-    uint32_t gt = 0, eq = 0;
-    for (int i = tid; i < len; i += kClThreads) {
-        const uint32_t key = s_keys[i];
-        gt += all || key > T;
-        eq += !all && key == T;
+    const int lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kClThreads / 32;
+    const int seg = (((len + kWarps - 1) / kWarps) + 31) & ~31;
+    const int s0 = min(len, warp * seg), s1 = min(len, s0 + seg);
+    __shared__ uint32_t s_wgt[kWarps], s_weq[kWarps], s_base[2];
+    uint32_t wgt = 0, weq = 0;
+    for (int b = s0; b < s1; b += 32) {
+        const int i = b + lane;
+        const uint32_t key = i < s1 ? s_keys[i] : 0u;
+        wgt += __popc(__ballot_sync(0xffffffffu, i < s1 && (all || key > T)));
+        weq += __popc(__ballot_sync(0xffffffffu, i < s1 && !all && key == T));
     }
-    uint32_t gt_tot, eq_tot;
-    scan512(gt, s_warp, &gt_tot);
-    scan512(eq, s_warp, &eq_tot);
-    if (tid == 0) { gcnt[2 * rank] = gt_tot; gcnt[2 * rank + 1] = eq_tot; }
-    cluster.sync();
-    uint32_t gt_before = 0, eq_before = 0;
-    for (int rr = 0; rr < rank; ++rr) {
-        gt_before += __ldcg(gcnt + 2 * rr);
-        eq_before += __ldcg(gcnt + 2 * rr + 1);
+    if (lane == 0) { s_wgt[warp] = wgt; s_weq[warp] = weq; }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t g = 0, e = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t a = s_wgt[w], c = s_weq[w];
+            s_wgt[w] = g; s_weq[w] = e;            // exclusive prefixes within the CTA
+            g += a; e += c;
+        }
+        gcnt[2 * rank] = g;
+        gcnt[2 * rank + 1] = e;
     }
-    uint32_t out_base = gt_before + min(eq_before, (uint32_t)(all ? 0 : k_rem));
-    uint32_t eq_base = eq_before;
+    cluster.sync();                                              // every CTA's counts are out
+    if (tid == 0) {
+        uint32_t g = 0, e = 0;
+        for (int rr = 0; rr < rank; ++rr) { g += __ldcg(gcnt + 2 * rr); e += __ldcg(gcnt + 2 * rr + 1); }
+        s_base[0] = g; s_base[1] = e;
+    }
+    __syncthreads();
+    uint32_t g = s_base[0] + s_wgt[warp], e = s_base[1] + s_weq[warp];
+    const uint32_t kr = all ? 0u : (uint32_t)k_rem;
+    const uint32_t lt = (1u << lane) - 1u;
     int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
     const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
-    for (int c0 = 0; c0 < len; c0 += kClThreads * 4) {
-        const int i0 = c0 + tid * 4;
-        uint32_t sel = 0, eqm = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (i0 + j < len) {
-                const uint32_t key = s_keys[i0 + j];
-                if (all || key > T) sel |= 1u << j;
-                else if (key == T) eqm |= 1u << j;
-            }
+    for (int b = s0; b < s1; b += 32) {
+        const int i = b + lane;
+        const uint32_t key = i < s1 ? s_keys[i] : 0u;
+        const bool is_gt = i < s1 && (all || key > T);
+        const bool is_eq = i < s1 && !all && key == T;
+        const uint32_t mg = __ballot_sync(0xffffffffu, is_gt);
+        const uint32_t me = __ballot_sync(0xffffffffu, is_eq);
+        const uint32_t my_g = g + __popc(mg & lt), my_e = e + __popc(me & lt);
+        uint32_t slot = 0xffffffffu;
+        if (is_gt) slot = my_g + min(my_e, kr);
+        else if (is_eq && my_e < kr) slot = my_g + my_e;
+        if (slot < (uint32_t)p.k) {
+            const int64_t ii = lo + i;
+            out[slot] = pb ? 8 * pb[ii >> 3] + (int32_t)(ii & 7) : (int32_t)ii;
         }
-        uint32_t et, ot;
-        uint32_t er = eq_base + scan512(__popc(eqm), s_warp, &et);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (eqm & (1u << j)) { if ((int32_t)er < k_rem) sel |= 1u << j; ++er; }
-        uint32_t slot = out_base + scan512(__popc(sel), s_warp, &ot);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (sel & (1u << j)) {
-                const int64_t ii = lo + i0 + j;
-                const int32_t pos = pb ? 8 * pb[ii >> 3] + (int32_t)(ii & 7) : (int32_t)ii;
-                if (slot < (uint32_t)p.k) out[slot] = pos;
-                ++slot;
-            }
-        }
-        eq_base += et;
-        out_base += ot;
+        g += __popc(mg);
+        e += __popc(me);
     }
 }
 
@@ -490,6 +526,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
 __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
                                   const int32_t *cnt, int32_t *pool_n, int nq)
 {
+    pdl_wait();
+    pdl_trigger();
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= nq) return;
     const int n = n_valid[q];
@@ -549,23 +587,21 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
         const size_t smem = (size_t)chunk * 4;
         cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(kClChunkMax * 4));
-        topk_cluster_kernel<<<dim3(kClusterCtas, nq), kClThreads, smem, st>>>(p);
-        note_launch();
-        return cudaGetLastError();
+        // the cluster shape comes from the kernel's __cluster_dims__
+        const cudaError_t e = launch_k(topk_cluster_kernel, dim3(kClusterCtas, nq), dim3(kClThreads),
+                                       smem, st, 0, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     const dim3 grid2(p.n_chunks, nq);
-    topk_init_kernel<<<nq, 256, 0, st>>>(p);
-    note_launch();
-    for (int r = 0; r < 3; ++r) {
-        topk_hist_kernel<<<grid2, kTkThreads, 0, st>>>(p, r);
-        topk_scan_kernel<<<nq, kTkThreads, 0, st>>>(p, r);
-        note_launch(2);
+    cudaError_t e = launch_k(topk_init_kernel, dim3(nq), dim3(256), 0, st, 0, p);
+    for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
+        e = launch_k(topk_hist_kernel, grid2, dim3(kTkThreads), 0, st, 0, p, r);
+        if (e == cudaSuccess) e = launch_k(topk_scan_kernel, dim3(nq), dim3(kTkThreads), 0, st, 0, p, r);
     }
-    topk_count_kernel<<<grid2, kTkThreads, 0, st>>>(p);
-    topk_offsets_kernel<<<nq, kTkThreads, 0, st>>>(p);
-    topk_write_kernel<<<grid2, kTkThreads, 0, st>>>(p);
-    note_launch(3);
-    return cudaGetLastError();
+    if (e == cudaSuccess) e = launch_k(topk_count_kernel, grid2, dim3(kTkThreads), 0, st, 0, p);
+    if (e == cudaSuccess) e = launch_k(topk_offsets_kernel, dim3(nq), dim3(kTkThreads), 0, st, 0, p);
+    if (e == cudaSuccess) e = launch_k(topk_write_kernel, grid2, dim3(kTkThreads), 0, st, 0, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_valid, int nq,
@@ -577,10 +613,10 @@ cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_v
     cudaError_t e = launch_topk(blockmax, ld_bm, n_valid, 1, nullptr, 0, nq, max_blocks,
                                 pool_blocks, pool_blk, pool_blocks, pool_n, ws, st);
     if (e != cudaSuccess) return e;
-    pool_count_kernel<<<(nq + 127) / 128, 128, 0, st>>>(n_valid, pool_blk, pool_blocks, pool_n,
-                                                         pool_n, nq);
-    note_launch();
-    return cudaGetLastError();
+    e = launch_k(pool_count_kernel, dim3((nq + 127) / 128), dim3(128), 0, st, 0,
+                 (const int32_t *)n_valid, (const int32_t *)pool_blk, pool_blocks,
+                 (const int32_t *)pool_n, pool_n, nq);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa2
