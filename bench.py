@@ -319,10 +319,25 @@ def run_csa2(args, rank, world):
 
 
 def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
-    """Pinned host inputs -> device -> layer call -> output back to the host."""
-    host = [{k_: v.cpu().pin_memory() for k_, v in step_inputs(wl, s, B, "cpu").items()}
-            for s in range(n_steps)]
-    dstage = {k_: torch.empty_like(v, device=dev) for k_, v in host[0].items()}
+    """Pinned host inputs -> device -> append + layer call -> output back to the
+    host.  A step's inputs travel packed in one buffer of a 4-slot pinned ring
+    (filled before the timed region, as a serving loop's staging ring would be)
+    with one host-to-device copy; the output comes back with one copy."""
+    order = ["C", "key", "q_idx", "w", "q"]
+    first = step_inputs(wl, 0, B, "cpu")
+    offs, nbytes = {}, 0
+    for k_ in order:
+        offs[k_] = nbytes
+        nbytes += (first[k_].numel() * first[k_].element_size() + 255) // 256 * 256
+    ring = [torch.empty(nbytes, dtype=torch.uint8).pin_memory() for _ in range(4)]
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def view(buf, k_):
+        t = first[k_]
+        n = t.numel() * t.element_size()
+        return buf[offs[k_]:offs[k_] + n].view(t.dtype).view(t.shape)
+
+    dstage = {k_: view(dbuf, k_) for k_ in order}
     qs = csa.Queries(list(range(B)), [T0] * B, 1, dev)
     idx = torch.empty(B, wl.k, dtype=torch.int32, device=dev)
     cnt = torch.empty(B, dtype=torch.int32, device=dev)
@@ -336,12 +351,15 @@ def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
     for s in range(n_steps):
+        slot = ring[s % len(ring)]
+        inp = step_inputs(wl, s, B, "cpu")
+        for k_ in order:
+            view(slot, k_).copy_(inp[k_])            # host-side staging, not timed
         qs.q_pos.copy_(base_len + s)      # the new token's position (after earlier appends)
         flush.fill_(1)
         torch.cuda.synchronize()
         e0.record()
-        for k_ in dstage:
-            dstage[k_].copy_(host[s][k_], non_blocking=True)
+        dbuf.copy_(slot, non_blocking=True)
         csa.quantize_append(cache, dstage["C"], None, dstage["key"])
         layer()
         out_h.copy_(out, non_blocking=True)
@@ -350,9 +368,8 @@ def run_e2e(csa, args, wl, cache, win, dev, n_steps, B, T0, world):
         if s >= args.warmup:
             times.append(e0.elapsed_time(e1) / 1e3)
     total = job_time(sum(times), world, dev)
-    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
     return {"value": round(job_value(B * args.steps, world, total), 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 4,
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": out_h.numel() * 4,
             "ms_per_step": round(total / args.steps * 1e3, 4)}
 
 
