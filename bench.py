@@ -441,6 +441,230 @@ def cpu_baseline(wl, cache, win, inp, t):
                       f"attention), {dt:.1f} s wall"}
 
 
+# ---------------------------------------------------------------- other workloads
+# Reindex decode at 1M, encoder prefill and the 20-layer decoder schedule: the
+# same library calls, timed as CUDA-graph replays with L2 flushed between steps.
+# They print their own JSON line (python bench.py --workload NAME); the default
+# line above is the 64K Full-mode decode.
+
+def timed_graphs(fns, steps, warmup, flush, before=None):
+    """One graph for the whole step and one per phase; returns (seconds per
+    step, seconds per phase)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=side):
+        for f in fns:
+            f()
+    gs = []
+    for f in fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            f()
+        gs.append(g)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+    tot = []
+    for s in range(warmup + steps):
+        if before:
+            before(s)
+        flush.fill_(s & 0xFF)
+        torch.cuda.synchronize()
+        ev[0].record()
+        g_all.replay()
+        ev[1].record()
+        torch.cuda.synchronize()
+        if s >= warmup:
+            tot.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    ph = np.zeros(len(fns))
+    n_ph = max(1, min(steps, 20))
+    for s in range(n_ph):
+        if before:
+            before(s)
+        flush.fill_(s & 0xFF)
+        torch.cuda.synchronize()
+        ev[0].record()
+        for i, g in enumerate(gs):
+            g.replay()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        ph += [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(len(fns))]
+    return sum(tot) / len(tot), ph / n_ph
+
+
+def _line(name, wl, args, world, value, unit, ms, phases, roofline, clocks, extra):
+    res = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "fp8 (indexer MMA), fp4/bf16 -> fp32 (attention)",
+           "data": "synthetic (seeded counter-hash generator)",
+           "config": {"workload": wl.name, "l2": "flushed between steps (512 MB write)",
+                      "graph": "one CUDA graph replay per step", "parallelism": f"replicas x{world}"},
+           "phases_us": {k: round(v * 1e6, 2) for k, v in phases.items()},
+           "roofline": roofline, "clocks": clocks.summary()}
+    res["config"].update(extra)
+    return res
+
+
+def run_reindex(csa, args, world, dev):
+    """Reindex layer over the 2,048 x 8 candidate pool at 1M context, 8 sequences."""
+    wl = ci.config(3)
+    B, T = wl.batch, wl.ctx_tokens[0]
+    cache = build_cache(csa, wl, dev, extra=8)
+    n = T                                          # entries visible to a query at position T - 1
+    qs = csa.Queries(list(range(B)), [T - 1] * B, 1, dev)
+    wcap = 512
+    win = ci.window_rows(wl, B, wcap, dev)
+    pool_blk = torch.zeros(B, 2048, dtype=torch.int32, device=dev)
+    pool_n = torch.zeros(B, dtype=torch.int32, device=dev)
+    qi0, w0, qa0 = ci.query_inputs(wl, B, dev, layer=0)
+    qi, w, qa = ci.query_inputs(wl, B, dev, layer=1)
+    idx = torch.zeros(B, wl.k, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, wl.heads, 512, device=dev)
+    counters = csa.new_counters(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # the Full layer that builds the pool (timed once, for context)
+    full = csa.Layer(csa.FULL, cache, qs, k=wl.k, q=qa0, win=win, n_win=wl.n_win, out=out,
+                     idx=idx, cnt=cnt, q_idx=qi0, w=w0, max_n=n, build_pool=True,
+                     pool_blk=pool_blk, pool_n=pool_n, counters=counters)
+    full()
+    torch.cuda.synchronize()
+    flush.fill_(1)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    full()
+    e1.record()
+    torch.cuda.synchronize()
+    full_us = e0.elapsed_time(e1) * 1e3
+    npool = 2048 * 8
+    scores = torch.empty(B, npool, device=dev)
+    nv = torch.empty(B, dtype=torch.int32, device=dev)
+    iws = csa.workspace(csa.index_workspace_size(B, 1, wl.h_idx, wl.d_idx), dev)
+    tws = csa.workspace(csa.topk_workspace_size(B, npool), dev)
+    aws = csa.workspace(csa.attn_workspace_size(B, wl.heads, wl.k, wl.n_win), dev)
+    fns = [lambda: csa.index_reindex(cache, qs, qi, w, pool_blk, pool_n, scores, n_valid=nv,
+                                     ws=iws, counters=counters),
+           lambda: csa.topk(scores, nv, wl.k, idx, cnt, max_n=npool, pool_blk=pool_blk, ws=tws),
+           lambda: csa.sparse_attn(cache, qs, idx, cnt, qa, win, wl.n_win, out, ws=aws,
+                                   counters=counters)]
+    clocks = Clocks(torch.cuda.current_device()).__enter__()
+    sec, ph = timed_graphs(fns, args.steps, args.warmup, flush)
+    clocks.__exit__(None, None, None)
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
+    pn = int(pool_n.sum())
+    hbm, _bf16, src = peaks()
+    ib = pn * IDX_BYTES_PER_ENTRY + B * 2048 * 4
+    roof = {"kernel": "index_main_kernel (Reindex, 8-row TMA boxes)", "bound": "hbm",
+            "achieved": round(ib / ph[0] / 1e9, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ib / ph[0] / 1e9 / hbm, 4), "peak_source": src, "traffic": None,
+            "algorithmic_bytes_per_launch": ib}
+    return _line("reindex", wl, args, world, B / sec, UNIT, sec * 1e3,
+                 {"index_reindex": ph[0], "topk_pool": ph[1], "sparse_attn": ph[2]}, roof, clocks,
+                 {"batch": B, "ctx_tokens": T, "m": 1, "pool_positions": pn // B, "k": wl.k,
+                  "heads": wl.heads, "full_layer_with_pool_us": round(full_us, 1)})
+
+
+def run_prefill(csa, args, world, dev):
+    """Encoder prefill chunk at m = 2: 4,096 causal queries after a 262,144-token
+    prefix; one Full layer (scoring all visible entries, top-2048, attention)
+    and five Reuse layers."""
+    wl = ci.config(4)
+    P, nq, m = wl.ctx_tokens[0], wl.q_per_seq, wl.m
+    cache = build_cache(csa, wl, dev, extra=nq // m + 8)
+    C, Z = ci.latent_rows(wl, 0, P, nq, dev)
+    key = ci.key_rows(wl, 0, P // m, nq // m, dev)
+    csa.quantize_append(cache, C[None].contiguous(), Z[None].contiguous(), key[None].contiguous(), seq=0)
+    q_pos = [P + i for i in range(nq)]
+    qs = csa.Queries([0] * nq, q_pos, wl.group, dev)
+    n_max = (P + nq) // m
+    ld = (n_max + 3) // 4 * 4
+    scores = torch.empty(nq, ld, device=dev)
+    nv = torch.empty(nq, dtype=torch.int32, device=dev)
+    idx = torch.zeros(nq, wl.k, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(nq, dtype=torch.int32, device=dev)
+    wcap = 8192
+    layers = []
+    for layer in range(6):
+        qi, w, qa = ci.query_inputs(wl, nq, dev, layer=layer)
+        layers.append(dict(qi=qi, w=w, qa=qa, win=ci.window_rows(wl, 1, wcap, dev, layer=layer),
+                           out=torch.empty(nq, wl.heads, 512, device=dev)))
+    counters = csa.new_counters(dev)
+    iws = csa.workspace(csa.index_workspace_size(nq, wl.group, wl.h_idx, wl.d_idx), dev)
+    tws = csa.workspace(csa.topk_workspace_size(nq, n_max), dev)
+    aws = csa.workspace(csa.attn_workspace_size(nq, wl.heads, wl.k, wl.n_win), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    L0 = layers[0]
+    fns = [lambda: csa.index_full(cache, qs, L0["qi"], L0["w"], n_max, scores, n_valid=nv, ws=iws,
+                                  counters=counters),
+           lambda: csa.topk(scores, nv, wl.k, idx, cnt, max_n=n_max, ws=tws),
+           lambda: csa.sparse_attn(cache, qs, idx, cnt, L0["qa"], L0["win"], wl.n_win, L0["out"],
+                                   ws=aws, counters=counters)]
+    for Ly in layers[1:]:
+        fns.append(lambda Ly=Ly: csa.sparse_attn(cache, qs, idx, cnt, Ly["qa"], Ly["win"], wl.n_win,
+                                                 Ly["out"], ws=aws, counters=counters))
+    clocks = Clocks(torch.cuda.current_device()).__enter__()
+    sec, ph = timed_graphs(fns, args.steps, args.warmup, flush)
+    clocks.__exit__(None, None, None)
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
+    pairs = sum((t + 1) // m for t in q_pos)              # (query, visible entry) pairs
+    flops = pairs * 2 * wl.h_idx * wl.d_idx
+    _hbm, bf16, src = peaks()
+    fp8 = 2.0 * bf16                                      # FP8 dense = 2 x bf16 (nominal ratio)
+    roof = {"kernel": "index_main_kernel (prefill, N = 32 queries x 8 heads)", "bound": "tensor",
+            "achieved": round(flops / ph[0] / 1e12, 1), "peak": round(fp8, 1), "unit": "TFLOP/s",
+            "frac": round(flops / ph[0] / 1e12 / fp8, 4),
+            "peak_source": f"{src} bf16 x 2 (nominal fp8/bf16 ratio)", "traffic": None,
+            "algorithmic_flops_per_launch": flops}
+    attn_flops = nq * 4 * wl.heads * 512 * (wl.k + wl.n_win)
+    phases = {"index_full": ph[0], "topk": ph[1], "sparse_attn_full": ph[2],
+              "sparse_attn_reuse_x5": float(sum(ph[3:]))}
+    res = _line("prefill", wl, args, world, nq * 6 / sec, "queries*layers/s", sec * 1e3, phases,
+                roof, clocks, {"queries": nq, "prefix_tokens": P, "m": m, "group": wl.group,
+                               "k": wl.k, "heads": wl.heads, "layers": "1 Full + 5 Reuse"})
+    res["attn_bf16_frac"] = round(attn_flops / ph[2] / 1e12 / bf16, 4)
+    return res
+
+
+def run_schedule(csa, args, world, dev):
+    """The 20-layer decoder (1 Full + 4 Reindex + 15 Reuse) over 64 sequences
+    with log-uniform contexts in [4,096, 1,048,576], one query each."""
+    from sparse_attention_decode_step_gb300 import schedule as S
+    base = ci.config(5)
+    lens = base.ctx_tokens
+    wl = ci.Workload(base.name, base.batch, lens, 0, 1, rms_norm=True, seed=base.seed)
+    cache = build_cache(csa, wl, dev, extra=8)
+    B = wl.batch
+    q_pos = [t - 1 for t in lens]
+    qs = csa.Queries(list(range(B)), q_pos, 1, dev)
+    wcap = 256
+    per_layer = []
+    for layer in range(20):
+        qi, w, qa = ci.query_inputs(wl, B, dev, layer=layer)
+        per_layer.append(dict(q_idx=qi, w=w, q=qa, win=ci.window_rows(wl, B, wcap, dev, layer=layer),
+                              out=torch.empty(B, wl.heads, 512, device=dev)))
+    counters = csa.new_counters(dev)
+    step = S.DecoderStep(csa, cache, qs, per_layer, k=wl.k, n_win=wl.n_win,
+                         max_n=max(lens), counters=counters)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fns = [step.layers[0]] + [lambda: [L() for L in step.layers[1:]]]
+    clocks = Clocks(torch.cuda.current_device()).__enter__()
+    sec, ph = timed_graphs(fns, args.steps, args.warmup, flush)
+    clocks.__exit__(None, None, None)
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
+    hbm, _bf16, src = peaks()
+    ib = sum(lens) * IDX_BYTES_PER_ENTRY
+    roof = {"kernel": "index_main_kernel (layer-1 Full scoring)", "bound": "hbm",
+            "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None, "peak_source": src,
+            "traffic": None, "algorithmic_bytes_full_layer": ib,
+            "note": "the Full layer's phase also holds its pool build, top-k and attention"}
+    return _line("schedule", wl, args, world, B * 20 / sec, "queries*layers/s", sec * 1e3,
+                 {"layer1_full_with_pool": ph[0], "layers2_20": ph[1]}, roof, clocks,
+                 {"batch": B, "ctx_tokens": "log-uniform [4096, 1048576]",
+                  "mean_ctx": int(sum(lens) / B), "layers": "1 Full + 4 Reindex + 15 Reuse",
+                  "k": wl.k, "heads": wl.heads})
+
+
 def run_reference(args, rank, world):
     """The float64 oracle, timed on the host cores, on the same workload."""
     if rank != 0:
@@ -498,6 +722,10 @@ def main():
                     help="profiling case: cached tokens per sequence instead of 65,535")
     ap.add_argument("--quick", action="store_true",
                     help="profiling case: skip the e2e and CPU-baseline legs")
+    ap.add_argument("--workload", default="decode_full",
+                    choices=["decode_full", "reindex", "prefill", "schedule"],
+                    help="decode_full (default): 32 x 64K Full-mode decode step; reindex: Reindex "
+                         "layer at 1M; prefill: m = 2 encoder chunk; schedule: 20-layer decoder")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -510,7 +738,13 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res = run_csa2(args, rank, world)
+    if args.workload == "decode_full":
+        res = run_csa2(args, rank, world)
+    else:
+        import sparse_attention_decode_step_gb300 as csa
+        dev = torch.device("cuda", torch.cuda.current_device())
+        run = {"reindex": run_reindex, "prefill": run_prefill, "schedule": run_schedule}
+        res = run[args.workload](csa, args, world, dev)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

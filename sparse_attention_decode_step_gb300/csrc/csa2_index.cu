@@ -29,6 +29,13 @@ namespace csa2 {
 constexpr int kIdxThreads = 192;
 constexpr int kTile = 128;
 constexpr int kEpiBatch = 4;          // tiles the epilogue takes per pass (decode)
+constexpr int kMaxGroupCols = 256;     // group * h_idx (the MMA's N) is at most 256
+
+// the four epilogue warps (2..5) only
+__device__ __forceinline__ void named_sync_epilogue()
+{
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
 
 struct IndexParams {
     const float *kscale;
@@ -142,6 +149,35 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
     }
 }
 
+// Scores of the queries in one 32-column pass of a group tile: query qq's HQ
+// head columns, ReLU, weighted sum with its w * scale, times the key scale.
+template <int HQ>
+__device__ __forceinline__ void group_scores(const IndexParams &p, const float (&v)[32],
+                                             const float *sWg, const int32_t *sNg, int c0, int nqp,
+                                             int q0, int64_t j, float sk, int lane)
+{
+#pragma unroll
+    for (int k2 = 0; k2 < 32 / HQ; ++k2) {
+        if (k2 >= nqp) break;
+        const int qq = c0 / HQ + k2;
+        const float *wq = sWg + qq * HQ;
+        float sc = 0.f;
+#pragma unroll
+        for (int h = 0; h < HQ; ++h) sc = fmaf(wq[h], fmaxf(v[k2 * HQ + h], 0.f), sc);
+        sc *= sk;
+        const bool valid = j < sNg[qq];
+        const int q = q0 + qq;
+        if (valid) p.scores[(int64_t)q * p.ld + j] = sc;
+        if (p.blockmax != nullptr) {
+            float bm = valid ? sc : -INFINITY;
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q * p.ld_bm + (j >> 3)] = bm;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- main kernel
 // Position in this CTA's unit range: group g, tile t of it, and gt = tiles of
 // group g (kept in a register: the global copy is read only on a group change).
@@ -161,8 +197,10 @@ __device__ __forceinline__ void unit_next(UnitIter &it, const int32_t *gtiles, i
     }
 }
 
-template <int D_IDX>
-__global__ void __launch_bounds__(kIdxThreads, 1)
+// kTwoPerSm: query groups run two CTAs per SM (registers capped to fit) so
+// that their epilogues, the bottleneck there, interleave; decode runs one.
+template <int D_IDX, bool kTwoPerSm>
+__global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
     index_main_kernel(const __grid_constant__ CUtensorMap tmap, IndexParams p, int stages, int nacc)
 {
     constexpr uint32_t kABytes = kTile * D_IDX;
@@ -186,6 +224,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     int *sI = reinterpret_cast<int *>(done + 1);             // misc ints
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sI + 8);
     int64_t *s_scan = reinterpret_cast<int64_t *>(s_tmem + 2);  // kIdxThreads
+    float *sWg = reinterpret_cast<float *>(s_scan + kIdxThreads);   // [group * h_idx] (group > 1)
+    int32_t *sNg = reinterpret_cast<int32_t *>(sWg + kMaxGroupCols); // [group]
 
     volatile int *abort_flag = sI;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -452,41 +492,37 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 if (lane == 0) count_event(p.counters, CSA2_CNT_TIMEOUT);
                 break;
             }
+            // a new query group: its w * scale and candidate counts into shared
+            // memory, once, by the four epilogue warps together
+            if (g != prev_g) {
+                named_sync_epilogue();               // the previous group's values are no longer read
+                const int etid = tid - 64;
+                for (int i = etid; i < p.group * p.h_idx; i += 128) sWg[i] = p.ws[(int64_t)q0 * p.h_idx + i];
+                for (int i = etid; i < p.group; i += 128) sNg[i] = p.nt[q0 + i];
+                named_sync_epilogue();
+                prev_g = g;
+            }
             tc_fence_after();
             const int64_t j = (int64_t)t * kTile + row;
             const float sk = sK[stage * kTile + row];
             const uint32_t tbase = tmem_base + ((quarter * 32u) << 16) + (uint32_t)acc * ncols_acc;
             {
-                // group of queries: h_idx columns per query, 16 columns per load
+                // h_idx columns per query; 32 columns (both TMEM loads in flight
+                // together) per pass; h_idx divides 16, so a pass holds whole queries
                 const int hq = p.h_idx;
-                for (int c0 = 0; c0 < p.group * hq; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + (uint32_t)c0, v);
+                const int ncols = p.group * hq;
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld16(tbase + (uint32_t)c0, *reinterpret_cast<float(*)[16]>(v));
+                    if (c0 + 16 < ncols) tmem_ld16(tbase + (uint32_t)c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
                     tmem_wait_ld();
-                    // columns c0..c0+15 cover queries c0/hq .. (c0+15)/hq (hq divides 16 or 16 divides hq)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
-                    if (hq <= 16) {
-                        const int per = 16 / hq;
-                        for (int k2 = 0; k2 < per; ++k2) {
-                            const int qq = c0 / hq + k2;
-                            if (qq >= p.group) break;
-                            const int q = q0 + qq;
-                            const float *wq = p.ws + (int64_t)q * hq;
-                            float s = 0.f;
-                            for (int h = 0; h < hq; ++h) s = fmaf(__ldg(wq + h), v[k2 * hq + h], s);
-                            s *= sk;
-                            const bool valid = j < __ldg(p.nt + q);
-                            if (valid) p.scores[(int64_t)q * p.ld + j] = s;
-                            if (p.blockmax != nullptr) {
-                                float bm = valid ? s : -INFINITY;
-                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-                                if ((lane & 7) == 0 && valid)
-                                    p.blockmax[(int64_t)q * p.ld_bm + (j >> 3)] = bm;
-                            }
-                        }
+                    const int nqp = min(32, ncols - c0) / hq;          // queries in this pass
+                    switch (hq) {
+                    case 1: group_scores<1>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
+                    case 2: group_scores<2>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
+                    case 4: group_scores<4>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
+                    case 8: group_scores<8>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
+                    default: group_scores<16>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
                     }
                 }
                 tc_fence_before();
@@ -518,7 +554,8 @@ static size_t index_smem_bytes(int d_idx, int n_pad, int stages, int nacc)
     const size_t k = (size_t)stages * kTile * 4;
     const size_t b = 2 * (((size_t)n_pad * d_idx + 1023) & ~(size_t)1023);
     const size_t bars = (size_t)(2 * stages + 4 + 2 * nacc + 1) * 8;
-    return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreads * 8;
+    return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreads * 8 +
+           kMaxGroupCols * 4 + kMaxGroupCols * 4;
 }
 
 size_t index_workspace_bytes(int nq, int group, int h_idx, int d_idx)
@@ -582,19 +619,22 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
     e = launch_k(index_prep_kernel, dim3(p.n_groups), dim3(256), 0, st, 0, p);
     if (e != cudaSuccess) return e;
 
-    const int stages = (p.n_pad <= 64) ? (c.d_idx == 128 ? 12 : 16) : 6;
-    const int nacc = (p.n_pad <= 64) ? 8 : 2;
+    // decode (N <= 64): one CTA per SM with a deep key pipeline (HBM-bound);
+    // query groups (N up to 256): two CTAs per SM, each with a shallow pipeline
+    // and one accumulator, whose MMAs and epilogues interleave
+    const bool grouped = p.n_pad > 64;
+    const int stages = grouped ? 2 : (c.d_idx == 128 ? 12 : 16);
+    const int nacc = grouped ? 1 : 8;
     const size_t smem = index_smem_bytes(c.d_idx, p.n_pad, stages, nacc);
-    const int grid = device_sm_count();
-    if (c.d_idx == 128) {
-        auto k = index_main_kernel<128>;
+    const int grid = device_sm_count() * (grouped ? 2 : 1);
+    auto run = [&](auto k) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        e = launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
-    } else {
-        auto k = index_main_kernel<64>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        e = launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
-    }
+        return launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
+    };
+    if (c.d_idx == 128)
+        e = grouped ? run(index_main_kernel<128, true>) : run(index_main_kernel<128, false>);
+    else
+        e = grouped ? run(index_main_kernel<64, true>) : run(index_main_kernel<64, false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
