@@ -418,12 +418,13 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
         while (it.u < it.u1) {
             const int g = it.g, t = it.t;
             const int q0 = g * p.group;
-            if (g != prev_g && p.group == 1) {
+            // (kTwoPerSm is only launched for groups of more than 64 / h_idx queries)
+            if (!kTwoPerSm && g != prev_g && p.group == 1) {
                 for (int h = 0; h < 16; ++h) wsr[h] = (h < p.h_idx) ? p.ws[(int64_t)q0 * p.h_idx + h] : 0.f;
                 ntq = p.nt[q0];
                 prev_g = g;
             }
-            if (p.group == 1) {
+            if (!kTwoPerSm && p.group == 1) {
                 // up to kEpiBatch consecutive tiles of this query per pass: all their
                 // TMEM loads are in flight together, one wait, one release each
                 int nb = 0, bt[kEpiBatch], bs[kEpiBatch], ba[kEpiBatch];
@@ -507,23 +508,37 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
             const float sk = sK[stage * kTile + row];
             const uint32_t tbase = tmem_base + ((quarter * 32u) << 16) + (uint32_t)acc * ncols_acc;
             {
-                // h_idx columns per query; 32 columns (both TMEM loads in flight
-                // together) per pass; h_idx divides 16, so a pass holds whole queries
+                // h_idx columns per query, 32 columns per pass (h_idx divides 16, so
+                // a pass holds whole queries); the next pass's TMEM loads are in
+                // flight while this pass is summed
                 const int hq = p.h_idx;
                 const int ncols = p.group * hq;
-                for (int c0 = 0; c0 < ncols; c0 += 32) {
-                    float v[32];
-                    tmem_ld16(tbase + (uint32_t)c0, *reinterpret_cast<float(*)[16]>(v));
-                    if (c0 + 16 < ncols) tmem_ld16(tbase + (uint32_t)c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-                    tmem_wait_ld();
-                    const int nqp = min(32, ncols - c0) / hq;          // queries in this pass
+                auto load32 = [&](int c, float (&v)[32]) {
+                    tmem_ld16(tbase + (uint32_t)c, *reinterpret_cast<float(*)[16]>(v));
+                    if (c + 16 < ncols) tmem_ld16(tbase + (uint32_t)c + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                };
+                auto sum32 = [&](int c, const float (&v)[32]) {
+                    const int nqp = min(32, ncols - c) / hq;          // queries in this pass
                     switch (hq) {
-                    case 1: group_scores<1>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
-                    case 2: group_scores<2>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
-                    case 4: group_scores<4>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
-                    case 8: group_scores<8>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
-                    default: group_scores<16>(p, v, sWg, sNg, c0, nqp, q0, j, sk, lane); break;
+                    case 1: group_scores<1>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
+                    case 2: group_scores<2>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
+                    case 4: group_scores<4>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
+                    case 8: group_scores<8>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
+                    default: group_scores<16>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
                     }
+                };
+                float va[32], vb[32];
+                load32(0, va);
+                tmem_wait_ld();
+                for (int c0 = 0; c0 < ncols; c0 += 64) {
+                    const bool has_b = c0 + 32 < ncols, has_a = c0 + 64 < ncols;
+                    if (has_b) load32(c0 + 32, vb);
+                    sum32(c0, va);
+                    if (!has_b) break;
+                    tmem_wait_ld();
+                    if (has_a) load32(c0 + 64, va);
+                    sum32(c0 + 32, vb);
+                    if (has_a) tmem_wait_ld();
                 }
                 tc_fence_before();
                 __syncwarp();
