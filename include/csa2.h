@@ -223,7 +223,10 @@ csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const i
  *   idx [nq][ld_idx] entry numbers < N_i (others are skipped and counted);
  *   q [nq][H][512] bf16 bits; H in {16, 32, 48, 64};
  *   win [batch][wcap][512] bf16 bits (NULL allowed when n_win == 0);
- *   out [nq][H][512] fp32; k_max >= every cnt[i]. */
+ *   out [nq][H][512] fp32; k_max >= every cnt[i].
+ * The attention needs no workspace (csa2_attn_workspace_size() is 0; the
+ * argument may be NULL): a query's row tiles are divided over at most 8 CTAs
+ * of one thread-block cluster, which merge on chip. */
 csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *queries,
                              const int32_t *idx, int64_t ld_idx, const int32_t *cnt,
                              int32_t k_max, const uint16_t *q, int32_t H, const uint16_t *win,

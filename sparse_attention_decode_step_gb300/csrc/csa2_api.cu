@@ -65,8 +65,9 @@ cudaError_t make_tmap_rows_u8(CUtensorMap *map, const void *base, int64_t rows, 
 
 // ---------------------------------------------------------------- attention plan
 // Rows of a query are processed in 128-row tiles; a query's tiles are divided
-// over `splits` CTAs so that the grid fills the SMs in one wave (one CTA per
-// SM: the kernel uses ~215 KB of shared memory and all 512 TMEM columns).
+// over `splits` CTAs (one thread-block cluster, at most 8) so that the grid
+// fills the SMs in one wave (one CTA per SM: the kernel uses ~215 KB of shared
+// memory and all 512 TMEM columns).
 int attn_plan(int nq, int k_max, int n_win)
 {
     const int rows = k_max + n_win > 0 ? k_max + n_win : 1;
@@ -74,16 +75,17 @@ int attn_plan(int nq, int k_max, int n_win)
     const int sms = device_sm_count();
     int s = sms / (nq > 0 ? nq : 1);
     if (s > tiles) s = tiles;
-    if (s > 152) s = 152;                  // the combine kernel holds at most 152 split weights
+    if (s > 8) s = 8;                      // the splits of a query merge within one cluster
     if (s < 1) s = 1;
     return s;
 }
 
+// The splits of a query merge on chip (distributed shared memory): the
+// attention needs no workspace.
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win)
 {
-    const int splits = attn_plan(nq, k_max, n_win);
-    return align_up((size_t)nq * splits * H * CSA2_D * 4, 256) +
-           align_up((size_t)nq * splits * H * 2 * 4, 256);
+    (void)nq; (void)H; (void)k_max; (void)n_win;
+    return 0;
 }
 
 }  // namespace csa2
@@ -284,10 +286,10 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
     if (queries->nq == 0) return CSA2_OK;
     CSA2_REQUIRE(k_max >= 0 && n_win >= 0 && k_max + n_win >= 1, CSA2_ERR_INVALID_ARG);
     CSA2_REQUIRE(H >= 1 && H <= 64, CSA2_ERR_UNSUPPORTED);
-    CSA2_REQUIRE(q && out && workspace, CSA2_ERR_INVALID_ARG);
+    CSA2_REQUIRE(q && out, CSA2_ERR_INVALID_ARG);
     CSA2_REQUIRE(k_max == 0 || (idx && cnt && ld_idx >= k_max), CSA2_ERR_INVALID_ARG);
     CSA2_REQUIRE(n_win == 0 || (win && wcap >= n_win), CSA2_ERR_INVALID_ARG);
-    CSA2_REQUIRE(al16(q) && al16(out) && al16(workspace) && (idx == nullptr || al4(idx)) &&
+    CSA2_REQUIRE(al16(q) && al16(out) && (idx == nullptr || al4(idx)) &&
                      (cnt == nullptr || al4(cnt)) && (win == nullptr || al16(win)) &&
                      (win_start == nullptr || al4(win_start)) && (lse == nullptr || al4(lse)),
                  CSA2_ERR_ALIGN);
@@ -316,10 +318,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
     p.out = out;
     p.lse = lse;
     p.splits = attn_plan(p.nq, k_max, n_win);
-    uint8_t *w = static_cast<uint8_t *>(workspace);
-    p.part_o = reinterpret_cast<float *>(w);
-    w += align_up((size_t)p.nq * p.splits * H * CSA2_D * 4, 256);
-    p.part_ml = reinterpret_cast<float *>(w);
+    (void)workspace;
     p.counters = counters;
     return cuda_status(launch_attn_tc(p, static_cast<cudaStream_t>(stream)));
 }

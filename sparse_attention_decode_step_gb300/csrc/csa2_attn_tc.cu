@@ -21,18 +21,17 @@
 // more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
 // in TMEM.
 //
-// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers, two per TMEM lane
-// quarter: a worker owns half of a tile row (256 channels to dequantise, 32
-// heads of its softmax; in the epilogue, 32 heads of one channel).  The
-// cross-row max reduction runs only when a logit exceeds its head's reference
-// max by more than 8 (always on the first tile); row sums are kept per thread
-// and reduced once.  Partials (O unnormalised [channel][head], reference max,
-// sum) are merged over the splits of a query in one of two ways.  Up to 8
-// splits form a thread-block cluster: each CTA stages its O^T in its own
-// shared memory, and after a cluster barrier every CTA sums, for its share of
-// the channels, the staged blocks of all splits read through distributed
-// shared memory, weighted by 2^(m_s - M) / L, and writes the output.  More
-// splits write partials to the workspace for the combine kernel.
+// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  The gather loads two
+// rows per warp instruction (lanes 0-15 one row, 16-31 the next, 16 code bytes
+// and 2 scale bytes per lane) and every lane dequantises what it loaded; in
+// the softmax a worker owns half of a tile row (32 heads), two per TMEM lane
+// quarter.  The cross-row max reduction runs only when a logit exceeds its
+// head's reference max by more than 8 (always on the first tile); row sums are
+// reduced once per tile.  The splits of a query (at most 8) form a thread-block
+// cluster: every CTA sends its reference max and sum to all peers, scales its
+// O^T by 2^(m_s - M) / L and stores each 32-channel chunk into the shared
+// memory of the CTA that owns the chunk, which sums the splits' chunks and
+// writes the output.  Nothing goes through global memory between splits.
 #include <cooperative_groups.h>
 
 #include "csa2_device.cuh"
@@ -282,7 +281,6 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-template <bool kCluster>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 {
     pdl_wait();
@@ -338,7 +336,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     if (tid < 64) { sM[tid] = -INFINITY; sAlpha[tid] = 1.f; sL[tid] = 0.f; }
     // a CTA's shared memory may be written by its cluster peers only once it runs:
     // arrive now, wait before the first remote store (the merge at the end)
-    if constexpr (kCluster) cluster_arrive();
+    cluster_arrive();
     if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
 
     // ---- Q: one bulk copy of the raw bf16 block [H][512] into the (still free)
@@ -662,42 +660,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             tc_fence_after();
         }
         if (!ok) *abort_flag = 1;
-        if constexpr (!kCluster) {
-            const int64_t pbase = (int64_t)q * p.splits + split;
-            if (ok) {
-                float *po = p.part_o + pbase * CSA2_D * H;
-#pragma unroll 1
-                for (int mb = 0; mb < 4; ++mb) {
-                    float o[32];
-                    if (n_tiles > 0) {
-                        tmem_ld32(tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16), o);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < 32; ++h) o[h] = 0.f;
-                    }
-                    float *dst = po + (int64_t)(128 * mb + row) * H + h0;
-                    if (h0 + 32 <= H) {
-#pragma unroll
-                        for (int h4 = 0; h4 < 8; ++h4)
-                            reinterpret_cast<float4 *>(dst)[h4] =
-                                make_float4(o[4 * h4], o[4 * h4 + 1], o[4 * h4 + 2], o[4 * h4 + 3]);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < 32; ++h)
-                            if (h0 + h < H) dst[h] = o[h];
-                    }
-                }
-                if (wt < H) {
-                    p.part_ml[(pbase * H + wt) * 2] = (n_tiles > 0) ? sM[wt] : -INFINITY;
-                    p.part_ml[(pbase * H + wt) * 2 + 1] = (n_tiles > 0) ? sL[wt] : 0.f;
-                }
-            }
-        }
         if (wt == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
     }
 
-    if constexpr (kCluster) {
+    {
         // ---- merge of the cluster's splits.  Every thread of every CTA reaches
         // each cluster barrier exactly once, whatever happened above.  32-channel
         // chunk c belongs to CTA c % S; each CTA scales its O^T block by
@@ -784,81 +750,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     }
 }
 
-// Merges the splits of each query: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
-// lse = (M + log2 L) ln 2.  Block = (query, 32 channels); partials [split][channel][head].
-// The per-split weights are computed once into shared memory; every thread then
-// sums its elements over the splits with independent loads.
-constexpr int kCombineMaxSplits = 152;   // static shared memory stays under 48 KB
-
-__global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p)
-{
-    pdl_wait();
-    pdl_trigger();
-    const int q = blockIdx.y, c0 = blockIdx.x * 32;
-    const int H = p.H, tid = threadIdx.x, S = p.splits;
-    __shared__ float sW[kCombineMaxSplits][64];   // weight of split s for head h
-    __shared__ float sInv[64];
-    __shared__ float sOut[32][65];                // [channel][head]
-    const float *ml = p.part_ml + (int64_t)q * S * H * 2;
-    if (tid < H) {
-        float M = -INFINITY;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((int64_t)s * H + tid) * 2]);
-        float L = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float ms = ml[((int64_t)s * H + tid) * 2];
-            const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-            sW[s][tid] = w;
-            L = fmaf(ml[((int64_t)s * H + tid) * 2 + 1], w, L);
-        }
-        sInv[tid] = (L > 0.f) ? 1.f / L : 0.f;
-        if (p.lse != nullptr && blockIdx.x == 0)
-            p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    __syncthreads();
-    const float *src = p.part_o + ((int64_t)q * S * CSA2_D + c0) * H;   // split 0, channel c0
-    const int64_t split_stride = (int64_t)CSA2_D * H;
-    for (int e = tid; e < 32 * H; e += 256) {
-        const int h = e % H;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int s = 0;
-        for (; s + 4 <= S; s += 4) {
-            a0 = fmaf(__ldg(src + (s + 0) * split_stride + e), sW[s + 0][h], a0);
-            a1 = fmaf(__ldg(src + (s + 1) * split_stride + e), sW[s + 1][h], a1);
-            a2 = fmaf(__ldg(src + (s + 2) * split_stride + e), sW[s + 2][h], a2);
-            a3 = fmaf(__ldg(src + (s + 3) * split_stride + e), sW[s + 3][h], a3);
-        }
-        for (; s < S; ++s) a0 = fmaf(__ldg(src + s * split_stride + e), sW[s][h], a0);
-        sOut[e / H][h] = ((a0 + a1) + (a2 + a3)) * sInv[h];
-    }
-    __syncthreads();
-    for (int i = tid; i < 32 * H; i += 256) {      // out[q][h][c0 + c]: 32 channels per head
-        const int h = i / 32, c = i % 32;
-        p.out[((int64_t)q * H + h) * CSA2_D + c0 + c] = sOut[c][h];
-    }
-}
-
-bool attn_uses_cluster(int splits) { return splits <= kMaxClusterSplits; }
-
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
     // receive area: ceil(16 / S) chunk slots x S senders blocks, largest at S = 7 (21)
     static_assert(21 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
     static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
+    if (p.splits < 1 || p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
     const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
                         kMaxClusterSplits * 2 * 64 * 4 + 6 * 8 + 64;
-    if (attn_uses_cluster(p.splits)) {
-        cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const cudaError_t e = launch_k(attn_tc_kernel<true>, dim3(p.splits, p.nq), dim3(kTcThreads),
-                                       smem, st, (unsigned)p.splits, p);
-        return e != cudaSuccess ? e : cudaGetLastError();
-    }
-    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaError_t e = launch_k(attn_tc_kernel<false>, dim3(p.splits, p.nq), dim3(kTcThreads), smem, st,
-                             0, p);
-    if (e != cudaSuccess) return e;
-    e = launch_k(attn_combine_kernel, dim3(CSA2_D / 32, p.nq), dim3(256), 0, st, 0, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = launch_k(attn_tc_kernel, dim3(p.splits, p.nq), dim3(kTcThreads), smem, st,
+                                   (unsigned)p.splits, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa2

@@ -292,15 +292,17 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
     it0.u1 = reinterpret_cast<int64_t *>(sI + 2)[1];
 
     if (warp == 0) {
-        // ================================================= TMA producer
-        if (lane == 0 && it0.u < it0.u1) {
+        // ================================================= TMA producer (whole warp:
+        // lane 0 issues the Full-mode copies; in Reindex mode lane i fetches the
+        // tile's pool block i)
+        if (it0.u < it0.u1) {
             UnitIter it = it0;
             int stage = 0;
             uint32_t phase = 0;
             int prev_g = -1, bidx = 1;
             uint32_t buse[2] = {0, 0};
             int64_t n_issued = 0;
-            int b = 0;
+            int b = 0, pn = 0;
             int64_t base = 0, room = 0;
             while (it.u < it.u1) {
                 const int g = it.g, t = it.t;
@@ -309,61 +311,67 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                     b = p.q_seq[q0];
                     base = p.seq_base[b];
                     room = p.seq_base[b + 1] - base;
+                    if (p.pool_blk != nullptr) pn = p.nt[q0];     // group == 1 in Reindex mode
                     bidx ^= 1;
-                    if (!mbar_wait(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)) break;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)))
+                        break;
                     ++buse[bidx];
-                    mbar_arrive_expect_tx(&bfull[bidx], b_bytes);
-                    bulk_load(sB + bidx * b_stride, p.q8img + (int64_t)g * b_bytes, b_bytes,
-                              &bfull[bidx]);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bfull[bidx], b_bytes);
+                        bulk_load(sB + bidx * b_stride, p.q8img + (int64_t)g * b_bytes, b_bytes,
+                                  &bfull[bidx]);
+                    }
                     prev_g = g;
                 }
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, abort_flag))) break;
                 uint8_t *dstA = sA + stage * kABytes;
                 float *dstK = sK + stage * kTile;
                 if (p.pool_blk == nullptr) {
-                    const int64_t r0 = base + (int64_t)t * kTile;
-                    int64_t nk = p.cap - r0;
-                    nk = nk > kTile ? kTile : nk;               // cap % 8 == 0, r0 % 8 == 0
-                    mbar_arrive_expect_tx(&full[stage], kABytes + (uint32_t)nk * 4u);
-                    tma_load_2d(dstA, &tmap, 0, (int32_t)r0, &full[stage]);
-                    bulk_load(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage]);
+                    if (lane == 0) {
+                        const int64_t r0 = base + (int64_t)t * kTile;
+                        int64_t nk = p.cap - r0;
+                        nk = nk > kTile ? kTile : nk;               // cap % 8 == 0, r0 % 8 == 0
+                        mbar_arrive_expect_tx(&full[stage], kABytes + (uint32_t)nk * 4u);
+                        tma_load_2d(dstA, &tmap, 0, (int32_t)r0, &full[stage]);
+                        bulk_load(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage]);
+                    }
                 } else {
-                    const int q = q0;   // group == 1 in Reindex mode
-                    const int pn = p.nt[q];
                     const int nblk = (pn + 7) / 8;
                     const int bb0 = t * (kTile / 8);
                     const int nb = min(kTile / 8, nblk - bb0);
-                    int nvalid = 0;
-                    for (int i = 0; i < nb; ++i) {
-                        const int blk = p.pool_blk[(int64_t)q * p.pool_blocks + bb0 + i];
-                        if (blk >= 0 && 8LL * blk + 8 <= room) ++nvalid;
+                    const int blk = lane < nb ? p.pool_blk[(int64_t)q0 * p.pool_blocks + bb0 + lane] : -1;
+                    const bool ok_blk = lane < nb && blk >= 0 && 8LL * blk + 8 <= room;
+                    const uint32_t vmask = __ballot_sync(0xffffffffu, ok_blk);
+                    const uint32_t nvalid = (uint32_t)__popc(vmask);
+                    if (lane == 0) {
+                        if ((int)nvalid < nb) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+                        mbar_arrive_expect_tx(&full[stage], nvalid * (8u * D_IDX + 32u));
                     }
-                    if (nvalid < nb) count_event(p.counters, CSA2_CNT_BAD_INPUT);
-                    mbar_arrive_expect_tx(&full[stage], (uint32_t)nvalid * (8u * D_IDX + 32u));
-                    for (int i = 0; i < nb; ++i) {
-                        const int blk = p.pool_blk[(int64_t)q * p.pool_blocks + bb0 + i];
-                        if (blk < 0 || 8LL * blk + 8 > room) continue;
+                    __syncwarp();
+                    if (ok_blk) {
                         const int64_t r = base + 8LL * blk;
-                        tma_load_2d(dstA + i * 8 * D_IDX, &tmap, 0, (int32_t)r, &full[stage]);
-                        bulk_load(dstK + i * 8, p.kscale + r, 32u, &full[stage]);
+                        tma_load_2d(dstA + lane * 8 * D_IDX, &tmap, 0, (int32_t)r, &full[stage]);
+                        bulk_load(dstK + lane * 8, p.kscale + r, 32u, &full[stage]);
                     }
                 }
                 ++n_issued;
                 if (++stage == stages) { stage = 0; phase ^= 1u; }
                 unit_next(it, p.gtiles, p.n_groups);
             }
-            if (it.u < it.u1) { *abort_flag = 1; count_event(p.counters, CSA2_CNT_TIMEOUT); }
+            if (lane == 0 && it.u < it.u1) { *abort_flag = 1; count_event(p.counters, CSA2_CNT_TIMEOUT); }
             // no copy of ours may still be landing when the CTA exits: wait (bounded)
             // for the last arming of every stage (issue i used stage i % stages, its
             // (i / stages)-th arming) and of every query buffer
-            volatile int no_abort = 0;
-            for (int s = 0; s < stages; ++s) {
-                if (n_issued <= s) continue;
-                const int64_t last = s + (n_issued - 1 - s) / stages * stages;
-                mbar_wait(&full[s], (uint32_t)((last / stages) & 1), &no_abort);
+            if (lane == 0) {
+                volatile int no_abort = 0;
+                for (int s = 0; s < stages; ++s) {
+                    if (n_issued <= s) continue;
+                    const int64_t last = s + (n_issued - 1 - s) / stages * stages;
+                    mbar_wait(&full[s], (uint32_t)((last / stages) & 1), &no_abort);
+                }
+                for (int i = 0; i < 2; ++i)
+                    if (buse[i]) mbar_wait(&bfull[i], (buse[i] - 1u) & 1u, &no_abort);
             }
-            for (int i = 0; i < 2; ++i)
-                if (buse[i]) mbar_wait(&bfull[i], (buse[i] - 1u) & 1u, &no_abort);
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer

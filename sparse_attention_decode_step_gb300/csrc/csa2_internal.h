@@ -94,13 +94,11 @@ struct AttnParams {
     int n_win;
     float sm_scale;
     float *out, *lse;
-    float *part_o;      // [nq][splits][512][H]
-    float *part_ml;     // [nq][splits][H][2]
     int splits;         // CTAs per query; its tiles are divided evenly over them
     uint32_t *counters;
 };
 
-// Splits of the row set and the workspace they need.
+// Splits (CTAs, at most 8 = one cluster) per query, and the workspace (none).
 int attn_plan(int nq, int k_max, int n_win);
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win);
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
