@@ -437,34 +437,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         gj = lane < 16 ? entry(0, 16 * wg + sub) : -1;
         my_j = entry(0, row);
         gather(0);
-        // Every CTA gathers in step with the others, so each tile's gather is a burst
-        // of random rows from HBM that stalls the issuing warps.  Asking L2 for all
-        // rows of the later tiles now (bulk prefetches, nothing waits for them) turns
-        // those gathers into L2 hits.
-        // (the entries are read four at a time so that their loads overlap)
-        for (int g0 = r_begin + kRows + wt; g0 < r_end; g0 += 4 * kWorkers) {
-            int jj[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int g = g0 + u * kWorkers;
-                jj[u] = (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int g = g0 + u * kWorkers;
-                if (g >= r_end) break;
-                if (g < rs.cnt) {
-                    if (jj[u] >= 0 && jj[u] < rs.nt) {
-                        const int64_t r = rs.base + jj[u];
-                        bulk_prefetch_l2(p.codes + r * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-                        bulk_prefetch_l2(p.scales + r * CSA2_SCALE_BYTES, CSA2_SCALE_BYTES);
-                    }
-                } else {
-                    const int64_t pos = rs.lo + (g - rs.cnt);
-                    bulk_prefetch_l2(p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D, CSA2_D * 2);
-                }
-            }
-        }
         if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + sub) : -1;
     }
     {

@@ -138,13 +138,6 @@ __device__ __forceinline__ void pdl_trigger()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Bulk prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned, size % 16 == 0);
-// nothing is written to shared memory and nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
