@@ -304,6 +304,23 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
             int64_t n_issued = 0;
             int b = 0, pn = 0;
             int64_t base = 0, room = 0;
+            // Reindex: lane i's pool block of the tiles 0..3 ahead, loaded 4 tiles
+            // early so that these dependent reads overlap (rotated each tile)
+            const bool reindex = p.pool_blk != nullptr;
+            UnitIter la = it;
+            auto pool_load = [&](const UnitIter &u) -> int {
+                if (u.u >= u.u1) return -1;
+                const int qq = u.g * p.group;
+                const int nbq = min(kTile / 8, (p.nt[qq] + 7) / 8 - u.t * (kTile / 8));
+                return lane < nbq ? p.pool_blk[(int64_t)qq * p.pool_blocks + u.t * (kTile / 8) + lane] : -1;
+            };
+            int pb0 = -1, pb1 = -1, pb2 = -1, pb3 = -1;
+            if (reindex) {
+                pb0 = pool_load(la); unit_next(la, p.gtiles, p.n_groups);
+                pb1 = pool_load(la); unit_next(la, p.gtiles, p.n_groups);
+                pb2 = pool_load(la); unit_next(la, p.gtiles, p.n_groups);
+                pb3 = pool_load(la); unit_next(la, p.gtiles, p.n_groups);
+            }
             while (it.u < it.u1) {
                 const int g = it.g, t = it.t;
                 const int q0 = g * p.group;
@@ -339,7 +356,10 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                     const int nblk = (pn + 7) / 8;
                     const int bb0 = t * (kTile / 8);
                     const int nb = min(kTile / 8, nblk - bb0);
-                    const int blk = lane < nb ? p.pool_blk[(int64_t)q0 * p.pool_blocks + bb0 + lane] : -1;
+                    const int blk = pb0;
+                    pb0 = pb1; pb1 = pb2; pb2 = pb3;
+                    pb3 = pool_load(la);
+                    unit_next(la, p.gtiles, p.n_groups);
                     const bool ok_blk = lane < nb && blk >= 0 && 8LL * blk + 8 <= room;
                     const uint32_t vmask = __ballot_sync(0xffffffffu, ok_blk);
                     const uint32_t nvalid = (uint32_t)__popc(vmask);
