@@ -255,12 +255,26 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
         const int gs = min(tid * per, p.n_groups), ge = min(gs + per, p.n_groups);
         int64_t mine = 0;
         for (int g = gs; g < ge; ++g) mine += p.gtiles[g];
-        s_scan[tid] = mine;
+        // exclusive prefix of the per-thread counts: shuffles within each warp,
+        // then the 6 warp totals
+        int64_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_scan[warp] = incl;                // warp totals
         __syncthreads();
+        int64_t before = 0, T = 0;
+#pragma unroll
+        for (int w = 0; w < kIdxThreads / 32; ++w) {
+            const int64_t v = s_scan[w];
+            before += (w < warp) ? v : 0;
+            T += v;
+        }
+        __syncthreads();                                     // the warp totals are read
+        s_scan[tid] = before + incl - mine;
         if (tid == 0) {
-            int64_t acc = 0;
-            for (int i = 0; i < kIdxThreads; ++i) { int64_t v = s_scan[i]; s_scan[i] = acc; acc += v; }
-            const int64_t T = acc;
             const int64_t u0 = T * blockIdx.x / gridDim.x, u1 = T * (blockIdx.x + 1) / gridDim.x;
             reinterpret_cast<int64_t *>(sI + 2)[0] = u0;
             reinterpret_cast<int64_t *>(sI + 2)[1] = u1;
