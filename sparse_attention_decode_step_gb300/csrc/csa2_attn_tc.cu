@@ -694,15 +694,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                     for (int h = 0; h < 32; ++h) o[h] = 0.f;
                 }
                 const int c = 4 * mb + (int)quarter;
+                if (S == 1) {
+                    // a single split: its scaled O^T is the output (lane = channel)
+                    float *od = p.out + ((int64_t)q * H + h0) * CSA2_D + 32 * c + lane;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h)
+                        if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
+                    continue;
+                }
                 float *dst = cluster.map_shared_rank(sX, c % S) +
                              ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
 #pragma unroll
                 for (int h = 0; h < 32; ++h) dst[h * 32] = o[h] * f[h];
             }
         }
-        cluster.sync();              // every block has arrived at its owner
+        if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
         // chunks rank, rank + S, ...: lane = channel, one head per warp and item
-        const int n_own = (16 - rank + S - 1) / S;
+        const int n_own = S > 1 ? (16 - rank + S - 1) / S : 0;
         for (int it = warp; it < n_own * H; it += kTcThreads / 32) {
             const int k = it / H, h = it % H, c = rank + k * S;
             const float *src = sX + k * S * kXBlock + h * 32 + lane;
