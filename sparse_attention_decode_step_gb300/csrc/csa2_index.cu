@@ -13,11 +13,14 @@
 // thread owns one entry (one TMEM lane) and turns its N dot products into
 // `group` scores with the ReLU-weighted head sum, then reduces 8 lanes for the
 // block max.  At decode the kernel is bound by the key stream from HBM
-// (132 B per entry), so the pipeline is built to keep ~128 KB of TMA loads in
-// flight per SM; at prefill (group 32, N = 256) it is bound by the FP8 MMA.
+// (132 B per entry): one CTA per SM keeps ~200 KB of TMA loads in flight.
+// With query groups (prefill: group 32, N = 256) the epilogue's ReLU-weighted
+// head sums on the CUDA cores are the bound: a second instance runs two CTAs
+// per SM so that their epilogues interleave.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
-// TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
+// Warp roles (192 threads): warp 0 = TMA producer (the whole warp: in Reindex
+// mode lane i fetches pool block i of a tile), warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
 // Units of work are (query group, 128-entry tile); each CTA takes a contiguous
 // range of units so the query tile (B operand) is reloaded only when the group
 // changes.  Every wait is bounded in time (csa2::kWaitNs) and sets an abort flag.

@@ -1,13 +1,15 @@
 // csa2_topk.cu -- per-query top-k by radix select, and the candidate pool.
 //
 // Top-k: the k largest scores, ties to the lower position, listed ascending
-// (the tie rule is this library's reading; the pages only say "top-k").
+// (the tie rule is this library's reading; the pages give none).
 // Scores become order-preserving uint32 keys (-0 == +0).  Three histogram
 // rounds (11 + 11 + 10 bits) find the exact k-th key T and how many keys equal
 // to T are taken; a final ordered compaction writes every key > T and the
-// first (lowest-position) keys == T.  Work is split into 4096-candidate chunks
-// so a 1M-candidate query spreads over 256 CTAs; histograms are merged with
-// global atomics (no CTA ever waits on another).
+// first (lowest-position) keys == T.  Up to 256K candidates a query is one
+// cluster of 8 CTAs (keys in shared memory, cluster barriers between rounds);
+// above that the work is split into 4096-candidate chunks over many CTAs in
+// separate launches, histograms merged with global atomics (no CTA ever waits
+// on another).
 //
 // Pool ([Notes] section 3): the same selection over the block maxima of a Full
 // layer (k = 2,048 blocks), then the count of visible positions they hold.
