@@ -42,7 +42,11 @@ UNIT = "queries/s/layer"
 L2_FLUSH_BYTES = 512 << 20
 # algorithmic bytes of the Full-mode indexer per visible entry: 128 B FP8 key +
 # 4 B key scale read, 4 B score written
-IDX_BYTES_PER_ENTRY = 128 + 4 + 4
+IDX_BYTES_PER_ENTRY = 128 + 4 + 4     # FP8 key (d_idx = 128) + key scale + score
+
+
+def idx_bytes_per_entry(d_idx):
+    return d_idx + 4 + 4
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "index_main_decode_b32_ctx32768.md")
 
 
@@ -168,6 +172,9 @@ def run_csa2(args, rank, world):
     if args.ctx:
         wl.ctx_tokens = [args.ctx] * wl.batch
         wl.name = f"decode_full_b{wl.batch}_ctx{args.ctx + 1}"
+    if args.d_idx != 128:
+        wl.d_idx = args.d_idx
+        wl.name += f"_didx{args.d_idx}"
     B = wl.batch
     T0 = wl.ctx_tokens[0]
     n_steps = args.warmup + args.steps
@@ -302,9 +309,9 @@ def run_csa2(args, rank, world):
     # ---- roofline of the dominant kernel (Full-mode indexer)
     hbm, bf16, src = peaks()
     entries = B * (int(qs.q_pos[0]) + 1)                 # visible entries of those calls
-    idx_bytes = entries * IDX_BYTES_PER_ENTRY
+    idx_bytes = entries * idx_bytes_per_entry(wl.d_idx)
     achieved = idx_bytes / t_index / 1e9
-    traffic = profiled_bytes_per_entry()
+    traffic = profiled_bytes_per_entry() if wl.d_idx == 128 else None
     roof = {"kernel": "index_main_kernel (+ index_prep_kernel; one csa2_index_full call)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_source": src,
@@ -740,6 +747,8 @@ def main():
                     help="profiling case: cached tokens per sequence instead of 65,535")
     ap.add_argument("--quick", action="store_true",
                     help="profiling case: skip the e2e and CPU-baseline legs")
+    ap.add_argument("--d-idx", type=int, default=128, choices=[64, 128],
+                    help="indexer key width of the decode_full workload (64: the 890 B/token layout)")
     ap.add_argument("--workload", default="decode_full",
                     choices=["decode_full", "reindex", "prefill", "schedule"],
                     help="decode_full (default): 32 x 64K Full-mode decode step; reindex: Reindex "

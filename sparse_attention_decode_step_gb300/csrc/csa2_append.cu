@@ -47,15 +47,12 @@ __device__ __forceinline__ uint32_t fp4_code(float x, float s)
     return c;
 }
 
-__global__ void __launch_bounds__(256) append_kernel(csa2_cache cache, const float *__restrict__ C,
-                                                    const float *__restrict__ Z,
-                                                    const float *__restrict__ key, int n_tok,
-                                                    int n_ent, uint32_t *counters)
+// Entry e of sequence b (warp = b * n_ent + e), one 16-channel group per lane.
+__device__ __forceinline__ void append_entry(const csa2_cache &cache, const float *__restrict__ C,
+                                             const float *__restrict__ Z,
+                                             const float *__restrict__ key, int n_tok, int n_ent,
+                                             uint32_t *counters, int64_t warp, int lane)
 {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= (int64_t)cache.batch * n_ent) return;
     const int b = (int)(warp / n_ent), e = (int)(warp % n_ent);
     const int64_t base = cache.seq_base[b];
@@ -153,6 +150,40 @@ __global__ void __launch_bounds__(256) append_kernel(csa2_cache cache, const flo
     }
 }
 
+__global__ void __launch_bounds__(256) append_kernel(csa2_cache cache, const float *__restrict__ C,
+                                                    const float *__restrict__ Z,
+                                                    const float *__restrict__ key, int n_tok,
+                                                    int n_ent, uint32_t *counters)
+{
+    pdl_wait();
+    pdl_trigger();
+    append_entry(cache, C, Z, key, n_tok, n_ent, counters,
+                 ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
+}
+
+// Small appends (n_ent <= 8, e.g. one decode token): CTA b writes the entries
+// of sequence b, one warp each, then advances seq_len[b] itself (same room
+// test as append_entry), so no second launch is needed.
+__global__ void __launch_bounds__(256) append_commit_fused_kernel(csa2_cache cache,
+                                                                  const float *__restrict__ C,
+                                                                  const float *__restrict__ Z,
+                                                                  const float *__restrict__ key,
+                                                                  int n_tok, int n_ent,
+                                                                  uint32_t *counters)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x;
+    append_entry(cache, C, Z, key, n_tok, n_ent, counters,
+                 (int64_t)b * n_ent + (threadIdx.x >> 5), threadIdx.x & 31);
+    __syncthreads();                           // every warp has read seq_len[b] and written
+    if (threadIdx.x == 0) {
+        const int64_t room = cache.seq_base[b + 1] - cache.seq_base[b];
+        const int64_t len = cache.seq_len[b];
+        if (len >= 0 && len + n_ent <= room) cache.seq_len[b] = (int32_t)(len + n_ent);
+    }
+}
+
 // Advances seq_len after every entry of the batch was written (same room test
 // as append_kernel, so refused sequences stay unchanged).
 __global__ void append_commit_kernel(csa2_cache cache, int n_ent)
@@ -170,6 +201,11 @@ cudaError_t launch_append(const csa2_cache &c, const float *C, const float *Z, c
                           int n_tok, uint32_t *counters, cudaStream_t st)
 {
     const int n_ent = n_tok / c.m;
+    if (n_ent <= 8) {
+        const cudaError_t e = launch_k(append_commit_fused_kernel, dim3((unsigned)c.batch),
+                                       dim3(32 * n_ent), 0, st, 0, c, C, Z, key, n_tok, n_ent, counters);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const int64_t warps = (int64_t)c.batch * n_ent;
     const int64_t blocks = (warps * 32 + 255) / 256;
     cudaError_t e = launch_k(append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 0, c, C, Z,
