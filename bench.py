@@ -696,7 +696,7 @@ def run_reference(args, rank, world):
         return None
     import oracle as O
     wl = ci.config(2)
-    B_s = 4   # queries per step of the CPU sample
+    B_s = max(1, min(wl.batch, os.cpu_count() or 1))   # one query per host core per step
     T0 = wl.ctx_tokens[0]
     n = T0 + 1
     # the sample's caches: oracle-encoded entries of B_s sequences
