@@ -595,6 +595,11 @@ def run_prefill(csa, args, world, dev):
     prefix; one Full layer (scoring all visible entries, top-2048, attention)
     and five Reuse layers."""
     wl = ci.config(4)
+    if args.ctx or args.queries:                          # smaller profiling case
+        wl.ctx_tokens = [args.ctx or wl.ctx_tokens[0]]
+        wl.q_per_seq = wl.new_tokens = args.queries or wl.q_per_seq
+        assert wl.ctx_tokens[0] % wl.m == 0 and wl.q_per_seq % (wl.group * wl.m) == 0
+        wl.name = f"prefill_m{wl.m}_prefix{wl.ctx_tokens[0]}_q{wl.q_per_seq}"
     P, nq, m = wl.ctx_tokens[0], wl.q_per_seq, wl.m
     cache = build_cache(csa, wl, dev, extra=nq // m + 8)
     C, Z = ci.latent_rows(wl, 0, P, nq, dev)
@@ -744,7 +749,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
     ap.add_argument("--ctx", type=int, default=0,
-                    help="profiling case: cached tokens per sequence instead of 65,535")
+                    help="profiling case: cached tokens per sequence instead of 65,535 "
+                         "(prefill: prefix tokens instead of 262,144)")
+    ap.add_argument("--queries", type=int, default=0,
+                    help="profiling case, prefill: queries instead of 4,096 (a multiple of 64)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling case: skip the e2e and CPU-baseline legs")
     ap.add_argument("--d-idx", type=int, default=128, choices=[64, 128],

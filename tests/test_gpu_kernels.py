@@ -355,3 +355,18 @@ def test_attention_window_truncation_and_scale():
 def test_attention_counts_and_skips_bad_index():
     c = _attn_case(32, 500, [40, 40], 16, 32, seed=33, bad=True)
     assert c[csa.CNT_BAD_INPUT] == 1
+
+
+def test_attention_one_query_long_selection():
+    # One query, 8000 selected rows plus 128 window rows: 64 row tiles (the
+    # last one ragged) divided over the 8 CTAs of one cluster.
+    _attn_case(64, 10000, [8000], 128, 256, seed=34)
+
+
+def test_attention_more_queries_than_sms_single_split():
+    # More queries than SMs: each query is one CTA (no cluster merge), with
+    # empty, short and several-tile selections mixed.
+    rng = np.random.default_rng(35)
+    cnts = rng.integers(0, 257, size=156).tolist()
+    cnts[:3] = [0, 256, 1]
+    _attn_case(64, 256, cnts, 32, 64, seed=35)
