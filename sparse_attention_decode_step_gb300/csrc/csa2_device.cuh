@@ -82,14 +82,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same with a suspend-time hint: the thread may sleep up to `ns`
+// nanoseconds (or until the phase completes) instead of returning at once, so
+// that a waiting warp takes fewer issue slots from the warps that are working.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 20000;   // 64 polls: at most ~1.3 ms between limit checks
+
 // Returns false when the wait gave up (time or poll limit reached, or *abort set).
+// kSleep: poll with the suspend-time hint.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort_flag)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() {
+        return kSleep ? mbar_try_wait_sleep(bar, parity, kSleepHintNs) : mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 63u) == 0u) {
             if (*abort_flag) return false;
             if (global_ns() - t0 > kWaitNs) return false;
@@ -248,6 +273,39 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// c + a * b on two fp32 lanes at once (one packed f32x2 FMA, round to nearest)
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("{\n"
+        ".reg .b64 ra, rb, rc;\n"
+        "mov.b64 ra, {%1, %2};\n"
+        "mov.b64 rb, {%3, %4};\n"
+        "mov.b64 rc, {%5, %6};\n"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n"
+        "}\n"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
 }
 
 // ------------------------------------------------------------------ formats

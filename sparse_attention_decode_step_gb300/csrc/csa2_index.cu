@@ -29,15 +29,18 @@
 
 namespace csa2 {
 
-constexpr int kIdxThreads = 192;
+constexpr int kIdxThreads = 192;          // one CTA per SM: 4 epilogue warps
+constexpr int kIdxThreadsGrouped = 320;   // two CTAs per SM: 8 epilogue warps each
+constexpr int kIdxThreadsMax = kIdxThreadsGrouped;
 constexpr int kTile = 128;
 constexpr int kEpiBatch = 4;          // tiles the epilogue takes per pass (decode)
 constexpr int kMaxGroupCols = 256;     // group * h_idx (the MMA's N) is at most 256
 
-// the four epilogue warps (2..5) only
+// the epilogue warps (2 ..) only
+template <int kEpiThreads>
 __device__ __forceinline__ void named_sync_epilogue()
 {
-    asm volatile("bar.sync 2, 128;" ::: "memory");
+    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
 struct IndexParams {
@@ -152,21 +155,36 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
     }
 }
 
-// Scores of the queries in one 32-column pass of a group tile: query qq's HQ
+// Scores of the queries in one W-column pass of a group tile: query qq's HQ
 // head columns, ReLU, weighted sum with its w * scale, times the key scale.
-template <int HQ>
-__device__ __forceinline__ void group_scores(const IndexParams &p, const float (&v)[32],
+// (HQ a multiple of 4: the weights are read 4 at a time, sWg being 16-byte
+// aligned, and the even and odd heads are summed in the two halves of a packed
+// f32x2 FMA, then added.)
+template <int HQ, int W = 32>
+__device__ __forceinline__ void group_scores(const IndexParams &p, const float (&v)[W],
                                              const float *sWg, const int32_t *sNg, int c0, int nqp,
                                              int q0, int64_t j, float sk, int lane)
 {
 #pragma unroll
-    for (int k2 = 0; k2 < 32 / HQ; ++k2) {
+    for (int k2 = 0; k2 < W / HQ; ++k2) {
         if (k2 >= nqp) break;
         const int qq = c0 / HQ + k2;
         const float *wq = sWg + qq * HQ;
         float sc = 0.f;
+        if constexpr (HQ % 4 == 0) {
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int h = 0; h < HQ; ++h) sc = fmaf(wq[h], fmaxf(v[k2 * HQ + h], 0.f), sc);
+            for (int h = 0; h < HQ; h += 4) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(wq + h);
+                const float *x = v + k2 * HQ + h;
+                acc = fma_f32x2(make_float2(w4.x, w4.y), make_float2(fmaxf(x[0], 0.f), fmaxf(x[1], 0.f)), acc);
+                acc = fma_f32x2(make_float2(w4.z, w4.w), make_float2(fmaxf(x[2], 0.f), fmaxf(x[3], 0.f)), acc);
+            }
+            sc = acc.x + acc.y;
+        } else {
+#pragma unroll
+            for (int h = 0; h < HQ; ++h) sc = fmaf(wq[h], fmaxf(v[k2 * HQ + h], 0.f), sc);
+        }
         sc *= sk;
         const bool valid = j < sNg[qq];
         const int q = q0 + qq;
@@ -200,12 +218,16 @@ __device__ __forceinline__ void unit_next(UnitIter &it, const int32_t *gtiles, i
     }
 }
 
-// kTwoPerSm: query groups run two CTAs per SM (registers capped to fit) so
-// that their epilogues, the bottleneck there, interleave; decode runs one.
+// kTwoPerSm: query groups run two CTAs per SM (registers capped to fit), each
+// with eight epilogue warps (two per TMEM lane quarter, each taking half of the
+// group's columns), so that the epilogues, the bottleneck there, have four
+// warps per scheduler to interleave; decode runs one CTA with four.
 template <int D_IDX, bool kTwoPerSm>
-__global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
+__global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, kTwoPerSm ? 2 : 1)
     index_main_kernel(const __grid_constant__ CUtensorMap tmap, IndexParams p, int stages, int nacc)
 {
+    constexpr int kThreads = kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads;
+    constexpr int kEpiWarps = kThreads / 32 - 2;
     constexpr uint32_t kABytes = kTile * D_IDX;
     constexpr uint32_t kSbo = 8 * D_IDX;
     constexpr uint32_t kLayout = (D_IDX == 128) ? kLayoutSW128 : kLayoutSW64;
@@ -222,12 +244,16 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + 2 * b_stride);
     uint64_t *full = bars, *empty = bars + stages;
     uint64_t *bfull = empty + stages, *bempty = bfull + 2;
-    uint64_t *tfull = bempty + 2, *tempty = tfull + nacc;
-    uint64_t *done = tempty + nacc;
+    // kTwoPerSm: one TMEM accumulator whose two column halves (see csplit) each
+    // have their own full / empty barrier pair
+    const int nbar = kTwoPerSm ? 2 : nacc;
+    uint64_t *tfull = bempty + 2, *tempty = tfull + nbar;
+    uint64_t *done = tempty + nbar;
     int *sI = reinterpret_cast<int *>(done + 1);             // misc ints
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sI + 8);
-    int64_t *s_scan = reinterpret_cast<int64_t *>(s_tmem + 2);  // kIdxThreads
-    float *sWg = reinterpret_cast<float *>(s_scan + kIdxThreads);   // [group * h_idx] (group > 1)
+    int64_t *s_scan = reinterpret_cast<int64_t *>(s_tmem + 2);  // kThreads
+    float *sWg = reinterpret_cast<float *>(                              // [group * h_idx] (group > 1)
+        (reinterpret_cast<uintptr_t>(s_scan + kIdxThreadsMax) + 15) & ~(uintptr_t)15);
     int32_t *sNg = reinterpret_cast<int32_t *>(sWg + kMaxGroupCols); // [group]
 
     volatile int *abort_flag = sI;
@@ -235,12 +261,19 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
     const uint32_t ncols_acc = (uint32_t)p.n_pad;
     uint32_t tm_cols = 32;
     while (tm_cols < ncols_acc * nacc) tm_cols <<= 1;
+    // column split between the two epilogue halves (a multiple of 32, so whole
+    // queries on each side; used with eight epilogue warps)
+    const int ncols_q = p.group * p.h_idx;
+    const int csplit = min(ncols_q, (ncols_q + 63) / 64 * 32);
 
     if (tid == 0) {
         sI[0] = 0;
-        for (int s = 0; s < stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
+        for (int s = 0; s < stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + kEpiWarps); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bfull[i], 1); mbar_init(&bempty[i], 1); }
-        for (int i = 0; i < nacc; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 4); }
+        for (int i = 0; i < nbar; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], kTwoPerSm ? kEpiWarps / 2 : kEpiWarps);
+        }
         mbar_init(done, 1);
         fence_barrier_init();
         prefetch_tmap(&tmap);
@@ -254,7 +287,7 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
 
     // ---- this CTA's unit range [u0, u1) and its first (group, tile)
     {
-        const int per = (p.n_groups + kIdxThreads - 1) / kIdxThreads;
+        const int per = (p.n_groups + kThreads - 1) / kThreads;
         const int gs = min(tid * per, p.n_groups), ge = min(gs + per, p.n_groups);
         int64_t mine = 0;
         for (int g = gs; g < ge; ++g) mine += p.gtiles[g];
@@ -270,7 +303,7 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
         __syncthreads();
         int64_t before = 0, T = 0;
 #pragma unroll
-        for (int w = 0; w < kIdxThreads / 32; ++w) {
+        for (int w = 0; w < kThreads / 32; ++w) {
             const int64_t v = s_scan[w];
             before += (w < warp) ? v : 0;
             T += v;
@@ -347,7 +380,7 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                     room = p.seq_base[b + 1] - base;
                     if (p.pool_blk != nullptr) pn = p.nt[q0];     // group == 1 in Reindex mode
                     bidx ^= 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)))
+                    if (!__all_sync(0xffffffffu, mbar_wait<kTwoPerSm>(&bempty[bidx], (buse[bidx] & 1u) ^ 1u, abort_flag)))
                         break;
                     ++buse[bidx];
                     if (lane == 0) {
@@ -357,7 +390,7 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                     }
                     prev_g = g;
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, abort_flag))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait<kTwoPerSm>(&empty[stage], phase ^ 1u, abort_flag))) break;
                 uint8_t *dstA = sA + stage * kABytes;
                 float *dstK = sK + stage * kTile;
                 if (p.pool_blk == nullptr) {
@@ -424,23 +457,45 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                 if (g != prev_g) {
                     if (prev_g >= 0) mma_commit(&bempty[bidx]);
                     bidx ^= 1;
-                    if (!mbar_wait(&bfull[bidx], buse[bidx] & 1u, abort_flag)) break;
+                    if (!mbar_wait<kTwoPerSm>(&bfull[bidx], buse[bidx] & 1u, abort_flag)) break;
                     ++buse[bidx];
                     prev_g = g;
                 }
-                if (!mbar_wait(&full[stage], phase, abort_flag)) break;
-                if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag)) break;
-                tc_fence_after();
+                if (!mbar_wait<kTwoPerSm>(&full[stage], phase, abort_flag)) break;
                 const uint32_t a0 = smem_u32(sA + stage * kABytes);
                 const uint32_t b0 = smem_u32(sB + bidx * b_stride);
-                const uint32_t d = tmem_base + (uint32_t)acc * ncols_acc;
+                if constexpr (kTwoPerSm) {
+                    // columns [0, csplit) and [csplit, n_pad): separate MMAs and
+                    // barriers, so each epilogue half waits only for its own columns
+                    bool ok = true;
 #pragma unroll
-                for (int k = 0; k < D_IDX / 32; ++k) {
-                    mma_f8f6f4(d, smem_desc(a0 + 32 * k, 16, kSbo, kLayout),
-                               smem_desc(b0 + 32 * k, 16, kSbo, kLayout), idesc, k > 0);
+                    for (int h = 0; h < 2; ++h) {
+                        if (!mbar_wait<true>(&tempty[h], aphase ^ 1u, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t c0 = h ? (uint32_t)csplit : 0u;
+                        const uint32_t n = h ? (uint32_t)(p.n_pad - csplit) : (uint32_t)csplit;
+                        const uint32_t id = instr_desc(128, n, 0, 0, 0, 0);
+#pragma unroll
+                        for (int k = 0; k < D_IDX / 32; ++k) {
+                            mma_f8f6f4(tmem_base + c0, smem_desc(a0 + 32 * k, 16, kSbo, kLayout),
+                                       smem_desc(b0 + c0 * D_IDX + 32 * k, 16, kSbo, kLayout), id, k > 0);
+                        }
+                        mma_commit(&tfull[h]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&empty[stage]);
+                } else {
+                    if (!mbar_wait<kTwoPerSm>(&tempty[acc], aphase ^ 1u, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)acc * ncols_acc;
+#pragma unroll
+                    for (int k = 0; k < D_IDX / 32; ++k) {
+                        mma_f8f6f4(d, smem_desc(a0 + 32 * k, 16, kSbo, kLayout),
+                                   smem_desc(b0 + 32 * k, 16, kSbo, kLayout), idesc, k > 0);
+                    }
+                    mma_commit(&empty[stage]);
+                    mma_commit(&tfull[acc]);
                 }
-                mma_commit(&empty[stage]);
-                mma_commit(&tfull[acc]);
                 if (++stage == stages) { stage = 0; phase ^= 1u; }
                 if (++acc == nacc) { acc = 0; aphase ^= 1u; }
                 unit_next(it, p.gtiles, p.n_groups);
@@ -529,10 +584,11 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                 continue;
             }
             // warp-uniform waits: the TMEM loads below are .sync.aligned
-            bool ok = mbar_wait(&tfull[acc], aphase, abort_flag);
+            const int tb = kTwoPerSm ? (warp >= 6 ? 1 : 0) : acc;   // this warp's TMEM barrier pair
+            bool ok = mbar_wait<kTwoPerSm>(&tfull[tb], aphase, abort_flag);
             // the stage's TMA data (key scales) is complete: observe it directly
             // (already complete, and it cannot be re-armed before this warp releases it)
-            ok = ok && mbar_wait(&full[stage], sphase, abort_flag);
+            ok = ok && mbar_wait<kTwoPerSm>(&full[stage], sphase, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 *abort_flag = 1;
                 if (lane == 0) count_event(p.counters, CSA2_CNT_TIMEOUT);
@@ -541,11 +597,12 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
             // a new query group: its w * scale and candidate counts into shared
             // memory, once, by the four epilogue warps together
             if (g != prev_g) {
-                named_sync_epilogue();               // the previous group's values are no longer read
+                named_sync_epilogue<32 * kEpiWarps>();   // the previous group's values are no longer read
                 const int etid = tid - 64;
-                for (int i = etid; i < p.group * p.h_idx; i += 128) sWg[i] = p.ws[(int64_t)q0 * p.h_idx + i];
-                for (int i = etid; i < p.group; i += 128) sNg[i] = p.nt[q0 + i];
-                named_sync_epilogue();
+                for (int i = etid; i < p.group * p.h_idx; i += 32 * kEpiWarps)
+                    sWg[i] = p.ws[(int64_t)q0 * p.h_idx + i];
+                for (int i = etid; i < p.group; i += 32 * kEpiWarps) sNg[i] = p.nt[q0 + i];
+                named_sync_epilogue<32 * kEpiWarps>();
                 prev_g = g;
             }
             tc_fence_after();
@@ -555,15 +612,20 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
             {
                 // h_idx columns per query, 32 columns per pass (h_idx divides 16, so
                 // a pass holds whole queries); the next pass's TMEM loads are in
-                // flight while this pass is summed
-                const int hq = p.h_idx;
+                // flight while this pass is summed.  With eight epilogue warps, warps
+                // 2..5 take the columns below `split` (a multiple of 32) and 6..9 the rest.
+                const int hq = p.h_idx, hq_sh = __ffs(hq) - 1;    // h_idx is a power of two
                 const int ncols = p.group * hq;
+                int c_lo = 0, c_hi = ncols;
+                if (kEpiWarps == 8) {
+                    if (warp >= 6) c_lo = csplit; else c_hi = csplit;
+                }
                 auto load32 = [&](int c, float (&v)[32]) {
                     tmem_ld16(tbase + (uint32_t)c, *reinterpret_cast<float(*)[16]>(v));
-                    if (c + 16 < ncols) tmem_ld16(tbase + (uint32_t)c + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                    if (c + 16 < c_hi) tmem_ld16(tbase + (uint32_t)c + 16, *reinterpret_cast<float(*)[16]>(v + 16));
                 };
                 auto sum32 = [&](int c, const float (&v)[32]) {
-                    const int nqp = min(32, ncols - c) / hq;          // queries in this pass
+                    const int nqp = min(32, c_hi - c) >> hq_sh;       // queries in this pass
                     switch (hq) {
                     case 1: group_scores<1>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
                     case 2: group_scores<2>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
@@ -572,22 +634,39 @@ __global__ void __launch_bounds__(kIdxThreads, kTwoPerSm ? 2 : 1)
                     default: group_scores<16>(p, v, sWg, sNg, c, nqp, q0, j, sk, lane); break;
                     }
                 };
-                float va[32], vb[32];
-                load32(0, va);
-                tmem_wait_ld();
-                for (int c0 = 0; c0 < ncols; c0 += 64) {
-                    const bool has_b = c0 + 32 < ncols, has_a = c0 + 64 < ncols;
-                    if (has_b) load32(c0 + 32, vb);
-                    sum32(c0, va);
-                    if (!has_b) break;
-                    tmem_wait_ld();
-                    if (has_a) load32(c0 + 64, va);
-                    sum32(c0 + 32, vb);
-                    if (has_a) tmem_wait_ld();
+                if constexpr (kEpiWarps == 8) {
+                    // (registers are capped for two CTAs per SM: one pass in flight;
+                    // the other three warps of this scheduler hide the load)
+                    for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                        float va[32];
+                        if (c0 + 16 < c_hi) {
+                            tmem_ld32(tbase + (uint32_t)c0, va);
+                        } else {
+                            tmem_ld16(tbase + (uint32_t)c0, *reinterpret_cast<float(*)[16]>(va));
+                        }
+                        tmem_wait_ld();
+                        sum32(c0, va);
+                    }
+                } else {
+                    float va[32], vb[32];
+                    if (c_lo < c_hi) {
+                        load32(c_lo, va);
+                        tmem_wait_ld();
+                    }
+                    for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+                        const bool has_b = c0 + 32 < c_hi, has_a = c0 + 64 < c_hi;
+                        if (has_b) load32(c0 + 32, vb);
+                        sum32(c0, va);
+                        if (!has_b) break;
+                        tmem_wait_ld();
+                        if (has_a) load32(c0 + 64, va);
+                        sum32(c0 + 32, vb);
+                        if (has_a) tmem_wait_ld();
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (lane == 0) mbar_arrive(&tempty[tb]);
             }
             // this warp is done with the stage's key scales: its share of the release
             __syncwarp();
@@ -613,8 +692,8 @@ static size_t index_smem_bytes(int d_idx, int n_pad, int stages, int nacc)
     const size_t a = (size_t)stages * kTile * d_idx;
     const size_t k = (size_t)stages * kTile * 4;
     const size_t b = 2 * (((size_t)n_pad * d_idx + 1023) & ~(size_t)1023);
-    const size_t bars = (size_t)(2 * stages + 4 + 2 * nacc + 1) * 8;
-    return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreads * 8 +
+    const size_t bars = (size_t)(2 * stages + 4 + 2 * (nacc > 2 ? nacc : 2) + 1) * 8;
+    return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreadsMax * 8 + 16 +
            kMaxGroupCols * 4 + kMaxGroupCols * 4;
 }
 
@@ -689,7 +768,8 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
     const int grid = device_sm_count() * (grouped ? 2 : 1);
     auto run = [&](auto k) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        return launch_k(k, dim3(grid), dim3(kIdxThreads), smem, st, 0, tmap, p, stages, nacc);
+        return launch_k(k, dim3(grid), dim3(grouped ? kIdxThreadsGrouped : kIdxThreads), smem, st, 0,
+                        tmap, p, stages, nacc);
     };
     if (c.d_idx == 128)
         e = grouped ? run(index_main_kernel<128, true>) : run(index_main_kernel<128, false>);
