@@ -285,9 +285,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     float *sRedL = sL + 64;                   // [4 quarters][64 heads] tile row sums
     float *sML = sRedL + 4 * 64;              // cluster merge: [split][m | l][64 heads]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sML + kMaxClusterSplits * 2 * 64);
-    uint64_t *bar_v = bars, *bar_s = bars + 1, *bar_p = bars + 2, *bar_o = bars + 3;
-    uint64_t *bar_done = bars + 4, *bar_q = bars + 5;
-    int *sFlag = reinterpret_cast<int *>(bars + 6);   // [0] abort [1] rescale [2] bad [3] need max
+    uint64_t *bar_v = bars;                   // [4]: V channel chunk c stored
+    uint64_t *bar_s = bars + 4, *bar_p = bars + 5, *bar_o = bars + 6;
+    uint64_t *bar_done = bars + 7, *bar_q = bars + 8;
+    int *sFlag = reinterpret_cast<int *>(bars + 9);   // [0] abort [1] rescale [2] bad [3] need max
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sFlag + 4);
     volatile int *abort_flag = sFlag;
 
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int n_tiles = t_end - t_begin;
 
     if (tid == 0) {
-        mbar_init(bar_v, kWorkers / 32);
+        for (int c = 0; c < 4; ++c) mbar_init(&bar_v[c], kWorkers / 32);
         mbar_init(bar_s, 1);
         mbar_init(bar_p, kWorkers / 32);
         mbar_init(bar_o, 1);
@@ -336,36 +337,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int row = (int)(quarter * 32 + lane);       // tile row == TMEM lane of this thread
     const int half = (warp - 1) >> 2;                 // heads 32 half .. of its softmax
 
-    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15, two rows per
-    // load instruction: lanes 0-15 take row 2t, lanes 16-31 row 2t + 1 of pair t, and
-    // lane sub = lane & 15 holds channels 32 sub .. 32 sub + 31 of that row (16 code
-    // bytes, 2 scale bytes).  A warp load then touches 4 lines, not 32 (one per
-    // row), which keeps the load/store unit free for the shared-memory traffic of
-    // the softmax.  The next tile's codes are loaded while this tile is in flight.
+    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15, one 128-channel
+    // chunk c (atom columns 2c, 2c + 1) at a time, so that the QK product of chunk c
+    // runs while the later chunks are dequantised.  In load x (0, 1) of chunk c, lane l
+    // takes row 8x + (l >> 2) of the warp's 16 and channels 128c + 32 (l & 3) .. + 31
+    // (16 code bytes, 2 scale bytes) into register slot t = 2c + x; as soon as chunk c
+    // of this tile is stored, the slot is refilled with chunk c of the next tile.
     const int wg = warp - 1;
     const int sub = lane & 15;
-    uint4 gc[8];                  // codes of pair t
+    const int s4 = lane & 3;
+    uint4 gc[8];                  // codes of slot t
     uint32_t gsc[8];              // the two scale bytes of those channels
     uint32_t gkind = 0;           // bit t: FP4 row with data; bit 8 + t: window row
-    int gj = -1;                  // entry of row 16 wg + sub of the tile gathered next
+    int gj = -1;                  // lanes 0-15: entry of row 16 wg + lane of the tile loaded next
     auto tile_row = [&](int tile, int r) { return r_begin + tile * kRows + r; };
     // entry of tile row r (-1 for window rows and rows past the end)
     auto entry = [&](int tile, int r) {
         const int g = tile_row(tile, r);
         return (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
     };
-    auto gather = [&](int tile) {
-        gkind = 0;
+    auto load_chunk = [&](int tile, int c) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int slot = 2 * t + (lane >> 4);
-            const int g = tile_row(tile, 16 * wg + slot);
-            const int j = __shfl_sync(0xffffffffu, gj, slot);
+        for (int x = 0; x < 2; ++x) {
+            const int t = 2 * c + x;
+            const int rw = 8 * x + (lane >> 2);
+            const int g = tile_row(tile, 16 * wg + rw);
+            const int j = __shfl_sync(0xffffffffu, gj, rw);
+            gkind &= ~((1u << t) | (1u << (8 + t)));
             if (g < r_end && g < rs.cnt) {
                 if (j >= 0 && j < rs.nt) {
                     const int64_t r = rs.base + j;
-                    gc[t] = __ldg(reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES) + sub);
-                    gsc[t] = __ldg(reinterpret_cast<const uint16_t *>(p.scales + r * CSA2_SCALE_BYTES) + sub);
+                    gc[t] = __ldg(reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES) + 4 * c + s4);
+                    gsc[t] = __ldg(reinterpret_cast<const uint16_t *>(p.scales + r * CSA2_SCALE_BYTES) + 4 * c + s4);
                     gkind |= 1u << t;
                 } else {
                     sFlag[2] = 1;
@@ -375,22 +378,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             }
         }
     };
-    // Stores of one lane: its 32 channels are 4 16-byte chunks 4 (sub & 1) + m of
-    // atom column sub >> 1.  Store j writes chunk m = (j + atom) & 3, so that the
-    // 32 lanes of one store spread over all eight 16-byte bank groups.
-    auto put4 = [&](int r, const uint4 (&v)[4]) {
-        const int a = sub >> 1, ph = sub & 1;
+    // Chunk c of this warp's rows into sV.  A lane's 32 channels are the 16-byte
+    // pieces 4 (s4 & 1) .. + 3 of atom column 2c + (s4 >> 1); with 8 consecutive rows
+    // per store the 32 lanes hit each 16-byte bank group 4 times (4 wavefronts, the
+    // minimum for 512 bytes).
+    auto store_chunk = [&](int tile, int c) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int m = (j + a) & 3;
-            const uint4 x = (m & 2) ? ((m & 1) ? v[3] : v[2]) : ((m & 1) ? v[1] : v[0]);
-            *reinterpret_cast<uint4 *>(sV + a * kVAtom + sw128((uint32_t)r, (uint32_t)(4 * ph + m))) = x;
-        }
-    };
-    auto store_v = [&](int tile) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int r = 16 * wg + 2 * t + (lane >> 4);
+        for (int x = 0; x < 2; ++x) {
+            const int t = 2 * c + x;
+            const int r = 16 * wg + 8 * x + (lane >> 2);
             uint4 v[4];
             if (gkind & (1u << t)) {
                 const uint32_t p0 = scale_pair(gsc[t] & 0xFFu), p1 = scale_pair((gsc[t] >> 8) & 0xFFu);
@@ -401,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             } else if (gkind & (1u << (8 + t))) {
                 const int64_t pos = rs.lo + (tile_row(tile, r) - rs.cnt);
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 4 * sub;
+                    p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 16 * c + 4 * s4;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint4 raw = __ldg(src + k);
@@ -412,14 +408,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
             }
-            put4(r, v);
+            uint8_t *dst = sV + (2 * c + (s4 >> 1)) * kVAtom;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<uint4 *>(dst + sw128((uint32_t)r, (uint32_t)(4 * (s4 & 1) + m))) = v[m];
         }
     };
     int my_j = -1;                // entry of this thread's softmax row in the current tile
     if (warp > 0 && n_tiles > 0) {
         gj = lane < 16 ? entry(0, 16 * wg + sub) : -1;
         my_j = entry(0, row);
-        gather(0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) load_chunk(0, c);
         if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + sub) : -1;
     }
     {
@@ -451,15 +451,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             const uint32_t id_pv = instr_desc(128, kHeads, 0, 0, 1, 1);
             const uint32_t v0 = smem_u32(sV), q0 = smem_u32(sQ), p0 = smem_u32(sP);
             for (int i = 0; i < n_tiles; ++i) {
-                if (!mbar_wait(bar_v, i & 1, abort_flag)) { *abort_flag = 1; break; }
-                tc_fence_after();
+                bool run = true;
+                for (int c = 0; c < 4 && run; ++c) {
+                    // the K range of chunk c (channels 128c ..) as soon as it is stored
+                    if (!mbar_wait(&bar_v[c], i & 1, abort_flag)) { run = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < CSA2_D / 16; ++ks) {
-                    const uint32_t a = v0 + (ks >> 2) * kVAtom + (ks & 3) * 32;
-                    const uint32_t b = q0 + (ks >> 2) * kQAtom + (ks & 3) * 32;
-                    mma_f16(tS, smem_desc(a, 16, 1024, kLayoutSW128),
-                            smem_desc(b, 16, 1024, kLayoutSW128), id_qk, ks > 0);
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        const int ks = 8 * c + k8;
+                        const uint32_t a = v0 + (ks >> 2) * kVAtom + (ks & 3) * 32;
+                        const uint32_t b = q0 + (ks >> 2) * kQAtom + (ks & 3) * 32;
+                        mma_f16(tS, smem_desc(a, 16, 1024, kLayoutSW128),
+                                smem_desc(b, 16, 1024, kLayoutSW128), id_qk, ks > 0);
+                    }
                 }
+                if (!run) { *abort_flag = 1; break; }
                 mma_commit(bar_s);
                 if (!mbar_wait(bar_p, i & 1, abort_flag)) { *abort_flag = 1; break; }
                 tc_fence_after();
@@ -495,15 +501,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             }
             const int g_row = tile_row(i, row);
             const bool valid = g_row < r_end && (g_row >= rs.cnt || (my_j >= 0 && my_j < rs.nt));
-            store_v(i);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_v);
-            int my_j_next = -1;
-            if (i + 1 < n_tiles) {
-                gather(i + 1);
-                if (i + 2 < n_tiles) gj = lane < 16 ? entry(i + 2, 16 * wg + sub) : -1;
-                my_j_next = entry(i + 1, row);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                store_chunk(i, c);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_v[c]);
+            }
+            // the next tile's codes: chunks 0 and 1 while the QK product finishes,
+            // chunks 2 and 3 while the PV product runs (issuing these loads takes
+            // about as long as either product)
+            const bool more = i + 1 < n_tiles;
+            if (more) {
+                load_chunk(i + 1, 0);
+                load_chunk(i + 1, 1);
             }
 
             // ---- softmax of this row, heads h0 .. h0+31
@@ -598,6 +609,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p);
+            int my_j_next = -1;
+            if (more) {
+                load_chunk(i + 1, 2);
+                load_chunk(i + 1, 3);
+                if (i + 2 < n_tiles) gj = lane < 16 ? entry(i + 2, 16 * wg + sub) : -1;
+                my_j_next = entry(i + 1, row);
+            }
             // this tile's row sums: over the warp's 32 rows, then the 4 quarters
             warp_reduce32<false>(x, lane);
             sRedL[quarter * 64 + h0 + lane] = x[0];
@@ -720,7 +738,7 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
     static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
     if (p.splits < 1 || p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
     const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
-                        kMaxClusterSplits * 2 * 64 * 4 + 6 * 8 + 64;
+                        kMaxClusterSplits * 2 * 64 * 4 + 9 * 8 + 64;
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const cudaError_t e = launch_k(attn_tc_kernel, dim3(p.splits, p.nq), dim3(kTcThreads), smem, st,
                                    (unsigned)p.splits, p);
