@@ -21,11 +21,13 @@
 // more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
 // in TMEM.
 //
-// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  The gather loads two
-// rows per warp instruction (lanes 0-15 one row, 16-31 the next, 16 code bytes
-// and 2 scale bytes per lane) and every lane dequantises what it loaded; in
-// the softmax a worker owns half of a tile row (32 heads), two per TMEM lane
-// quarter.  The cross-row max reduction runs only when a logit exceeds its
+// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  V is gathered and
+// dequantised in four 128-channel chunks (8 rows x 64 code bytes per warp
+// load, 16 code bytes and 2 scale bytes per lane), each chunk with its own
+// barrier, so the QK product of chunk c runs while chunk c + 1 is stored; the
+// next tile's codes are loaded in two halves, during the tail of the QK
+// product and during the PV product.  In the softmax a worker owns half of a
+// tile row (32 heads), two per TMEM lane quarter.  The cross-row max reduction runs only when a logit exceeds its
 // head's reference max by more than 8 (always on the first tile); row sums are
 // reduced once per tile.  The splits of a query (at most 8) form a thread-block
 // cluster: every CTA sends its reference max and sum to all peers, scales its
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 bool run = true;
                 for (int c = 0; c < 4 && run; ++c) {
                     // the K range of chunk c (channels 128c ..) as soon as it is stored
-                    if (!mbar_wait(&bar_v[c], i & 1, abort_flag)) { run = false; break; }
+                    if (!mbar_wait<true>(&bar_v[c], i & 1, abort_flag)) { run = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int k8 = 0; k8 < 8; ++k8) {
@@ -467,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 }
                 if (!run) { *abort_flag = 1; break; }
                 mma_commit(bar_s);
-                if (!mbar_wait(bar_p, i & 1, abort_flag)) { *abort_flag = 1; break; }
+                if (!mbar_wait<true>(bar_p, i & 1, abort_flag)) { *abort_flag = 1; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int mb = 0; mb < 4; ++mb) {
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         bool ok = true;
         for (int i = 0; i < n_tiles && ok; ++i) {
             if (i > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (i - 1) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_o, (i - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             }
 
             // ---- softmax of this row, heads h0 .. h0+31
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_s, i & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             float x[32];
