@@ -712,16 +712,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             }
         }
         if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
-        // chunks rank, rank + S, ...: lane = channel, one head per warp and item
+        // chunks rank, rank + S, ...: lane = channel; a warp sums 4 heads per item
+        // (all their loads in flight together)
         const int n_own = S > 1 ? (16 - rank + S - 1) / S : 0;
-        for (int it = warp; it < n_own * H; it += kTcThreads / 32) {
-            const int k = it / H, h = it % H, c = rank + k * S;
-            const float *src = sX + k * S * kXBlock + h * 32 + lane;
-            float v[kMaxClusterSplits];
+        for (int it = warp; it < n_own * 16; it += kTcThreads / 32) {
+            const int k = it >> 4, hb = 4 * (it & 15), c = rank + k * S;
+            if (hb >= H) continue;
+            const float *src = sX + k * S * kXBlock + hb * 32 + lane;
+            float v[4][kMaxClusterSplits];
 #pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) v[s] = (s < S) ? src[s * kXBlock] : 0.f;
-            p.out[((int64_t)q * H + h) * CSA2_D + 32 * c + lane] =
-                ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+            for (int s = 0; s < kMaxClusterSplits; ++s)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j][s] = (s < S) ? src[s * kXBlock + j * 32] : 0.f;
+            float *od = p.out + ((int64_t)q * H + hb) * CSA2_D + 32 * c + lane;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (hb + j < H)
+                    od[(int64_t)j * CSA2_D] = ((v[j][0] + v[j][1]) + (v[j][2] + v[j][3])) +
+                                              ((v[j][4] + v[j][5]) + (v[j][6] + v[j][7]));
         }
     }
 
