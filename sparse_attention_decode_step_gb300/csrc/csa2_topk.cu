@@ -396,24 +396,36 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     __syncthreads();
 
     // keys of this CTA's candidates into shared memory (lo is a multiple of 4),
-    // with the first round's histogram (top 11 bits) built on the way
-    for (int i = tid * 4; i < len; i += kClThreads * 4) {
-        if (i + 4 <= len) {
-            const float4 f = *reinterpret_cast<const float4 *>(row + lo + i);
-            const uint32_t k0 = score_key(f.x), k1 = score_key(f.y);
-            const uint32_t k2 = score_key(f.z), k3 = score_key(f.w);
-            *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k0, k1, k2, k3);
-            if (!all) {
-                atomicAdd(&hist[k0 >> 21], 1u);
-                atomicAdd(&hist[k1 >> 21], 1u);
-                atomicAdd(&hist[k2 >> 21], 1u);
-                atomicAdd(&hist[k3 >> 21], 1u);
-            }
-        } else {
-            for (int j = i; j < len; ++j) {
-                const uint32_t kj = score_key(row[lo + j]);
-                s_keys[j] = kj;
-                if (!all) atomicAdd(&hist[kj >> 21], 1u);
+    // with the first round's histogram (top 11 bits) built on the way; a
+    // thread's loads of one pass (up to kLoadUnroll float4) are all in flight
+    // before the first is used
+    constexpr int kLoadUnroll = 4;
+    for (int i0 = tid * 4; i0 < len; i0 += kClThreads * 4 * kLoadUnroll) {
+        float4 f[kLoadUnroll];
+#pragma unroll
+        for (int u = 0; u < kLoadUnroll; ++u) {
+            const int i = i0 + u * kClThreads * 4;
+            if (i + 4 <= len) f[u] = *reinterpret_cast<const float4 *>(row + lo + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadUnroll; ++u) {
+            const int i = i0 + u * kClThreads * 4;
+            if (i + 4 <= len) {
+                const uint32_t k0 = score_key(f[u].x), k1 = score_key(f[u].y);
+                const uint32_t k2 = score_key(f[u].z), k3 = score_key(f[u].w);
+                *reinterpret_cast<uint4 *>(s_keys + i) = make_uint4(k0, k1, k2, k3);
+                if (!all) {
+                    atomicAdd(&hist[k0 >> 21], 1u);
+                    atomicAdd(&hist[k1 >> 21], 1u);
+                    atomicAdd(&hist[k2 >> 21], 1u);
+                    atomicAdd(&hist[k3 >> 21], 1u);
+                }
+            } else if (i < len) {
+                for (int j = i; j < len; ++j) {
+                    const uint32_t kj = score_key(row[lo + j]);
+                    s_keys[j] = kj;
+                    if (!all) atomicAdd(&hist[kj >> 21], 1u);
+                }
             }
         }
     }
@@ -425,6 +437,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
             const int pbits = r == 0 ? 0 : (r == 1 ? 11 : 22);
             const uint32_t nb = r == 2 ? 1024u : 2048u;
             if (r > 0) {                                         // round 0 was built with the load
+#pragma unroll 4
                 for (int i = tid; i < len; i += kClThreads) {
                     const uint32_t key = s_keys[i];
                     if ((key >> (32 - pbits)) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1u)], 1u);
@@ -473,6 +486,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     const int s0 = min(len, warp * seg), s1 = min(len, s0 + seg);
     __shared__ uint32_t s_wgt[kWarps], s_weq[kWarps], s_base[2];
     uint32_t wgt = 0, weq = 0;
+#pragma unroll 4
     for (int b = s0; b < s1; b += 32) {
         const int i = b + lane;
         const uint32_t key = i < s1 ? s_keys[i] : 0u;
@@ -503,6 +517,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     const uint32_t lt = (1u << lane) - 1u;
     int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
     const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
+#pragma unroll 4
     for (int b = s0; b < s1; b += 32) {
         const int i = b + lane;
         const uint32_t key = i < s1 ? s_keys[i] : 0u;
