@@ -381,9 +381,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         }
     };
     // Chunk c of this warp's rows into sV.  A lane's 32 channels are the 16-byte
-    // pieces 4 (s4 & 1) .. + 3 of atom column 2c + (s4 >> 1); with 8 consecutive rows
-    // per store the 32 lanes hit each 16-byte bank group 4 times (4 wavefronts, the
-    // minimum for 512 bytes).
+    // pieces 4 (s4 & 1) .. + 3 of atom column 2c + (s4 >> 1).  16-byte stores are
+    // served 8 lanes (2 rows x 4 slices) at a time; the lanes of the second atom
+    // column (hi) take their pieces in an order rotated by 2 (v[k] = piece
+    // (k + 2) & 3, so the code words and scale bytes are swapped on input), which
+    // puts the 8 lanes of each group on 8 different 16-byte bank groups.
+    const int hi = s4 >> 1;
     auto store_chunk = [&](int tile, int c) {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -391,18 +394,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             const int r = 16 * wg + 8 * x + (lane >> 2);
             uint4 v[4];
             if (gkind & (1u << t)) {
-                const uint32_t p0 = scale_pair(gsc[t] & 0xFFu), p1 = scale_pair((gsc[t] >> 8) & 0xFFu);
-                v[0] = fp4x8_to_f16(gc[t].x, p0);
-                v[1] = fp4x8_to_f16(gc[t].y, p0);
-                v[2] = fp4x8_to_f16(gc[t].z, p1);
-                v[3] = fp4x8_to_f16(gc[t].w, p1);
+                const uint32_t sc = hi ? (gsc[t] >> 8) | (gsc[t] << 8) : gsc[t];
+                const uint32_t p0 = scale_pair(sc & 0xFFu), p1 = scale_pair((sc >> 8) & 0xFFu);
+                const uint4 g = gc[t];
+                v[0] = fp4x8_to_f16(hi ? g.z : g.x, p0);
+                v[1] = fp4x8_to_f16(hi ? g.w : g.y, p0);
+                v[2] = fp4x8_to_f16(hi ? g.x : g.z, p1);
+                v[3] = fp4x8_to_f16(hi ? g.y : g.w, p1);
             } else if (gkind & (1u << (8 + t))) {
                 const int64_t pos = rs.lo + (tile_row(tile, r) - rs.cnt);
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 16 * c + 4 * s4;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint4 raw = __ldg(src + k);
+                    const uint4 raw = __ldg(src + ((k + 2 * hi) & 3));
                     v[k] = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
                                       bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
                 }
@@ -410,10 +415,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
             }
-            uint8_t *dst = sV + (2 * c + (s4 >> 1)) * kVAtom;
+            uint8_t *dst = sV + (2 * c + hi) * kVAtom;
 #pragma unroll
             for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4 *>(dst + sw128((uint32_t)r, (uint32_t)(4 * (s4 & 1) + m))) = v[m];
+                *reinterpret_cast<uint4 *>(
+                    dst + sw128((uint32_t)r, (uint32_t)(4 * (s4 & 1) + ((m + 2 * hi) & 3)))) = v[m];
         }
     };
     int my_j = -1;                // entry of this thread's softmax row in the current tile
