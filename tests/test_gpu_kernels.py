@@ -197,6 +197,32 @@ def test_index_full_grouped_prefill(exact):
             assert rel_rows(gs[i, :n][None], ref[None])[0] <= TOL
 
 
+@pytest.mark.parametrize("group,h_idx,d_idx", [(10, 8, 128), (6, 16, 64), (4, 4, 128)])
+def test_index_full_groups_uneven_column_halves(group, h_idx, d_idx):
+    # N = group * h_idx = 80 and 96: the two-CTA launch whose eight epilogue warps
+    # split the columns unevenly (64 + 16, 64 + 32; the second half's MMA is
+    # N = 16 or 32 and its B operand starts mid-tile); N = 16: a small group
+    # in the one-CTA launch.  Exact integer inputs: scores bit-exact.
+    wl = ci.Workload("t", 1, [6000], 0, 2, h_idx=h_idx, d_idx=d_idx, exact=True, seed=25)
+    cache = build_gpu_cache(wl, DEV)
+    nq = 2 * group
+    q_pos = [5960 - 3 * i for i in range(nq)]
+    qs = csa.Queries([0] * nq, q_pos, group, DEV)
+    qi, w, _ = ci.query_inputs(wl, nq, "cpu")
+    max_n = 3000
+    scores = torch.full((nq, max_n), float("nan"), device=DEV)
+    bm = torch.full((nq, (max_n // 8 + 3) // 4 * 4), float("nan"), device=DEV)
+    csa.index_full(cache, qs, qi.to(DEV), w.to(DEV), max_n, scores, blockmax=bm)
+    torch.cuda.synchronize()
+    oc = oracle_seq_cache(wl, 0, 3000)
+    gs, gb = _np(scores), _np(bm)
+    for i in range(nq):
+        n = (q_pos[i] + 1) // 2
+        ref = O.scores_full(oc["kidx"], oc["kscale"], qi[i].numpy(), w[i].numpy(), 0, n)
+        assert np.array_equal(gs[i, :n].astype(np.float64), ref), i
+        assert np.array_equal(gb[i, :(n + 7) // 8].astype(np.float64), O.blockmax(ref)), i
+
+
 @pytest.mark.parametrize("exact", [True, False])
 def test_index_reindex_pool(exact):
     n = 20000
