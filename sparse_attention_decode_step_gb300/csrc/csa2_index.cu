@@ -16,11 +16,14 @@
 // (132 B per entry): one CTA per SM keeps ~200 KB of TMA loads in flight.
 // With query groups (prefill: group 32, N = 256) the epilogue's ReLU-weighted
 // head sums on the CUDA cores are the bound: a second instance runs two CTAs
-// per SM so that their epilogues interleave.
+// per SM with eight epilogue warps each, so that four epilogue warps per
+// scheduler interleave; the two column halves of its accumulator are separate
+// MMAs with their own TMEM barriers.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (the whole warp: in Reindex
-// mode lane i fetches pool block i of a tile), warp 1 = MMA issuer and TMEM
-// owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32 (w % 4) ..).
+// Warp roles: warp 0 = TMA producer (the whole warp: in Reindex mode lane i
+// fetches pool block i of a tile), warp 1 = MMA issuer and TMEM owner, warps
+// 2.. = epilogue (warp w reads TMEM lanes 32 (w % 4) ..); 192 threads (four
+// epilogue warps) at decode, 320 (eight) with query groups.
 // Units of work are (query group, 128-entry tile); each CTA takes a contiguous
 // range of units so the query tile (B operand) is reloaded only when the group
 // changes.  Every wait is bounded in time (csa2::kWaitNs) and sets an abort flag.
@@ -155,18 +158,18 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
     }
 }
 
-// Scores of the queries in one W-column pass of a group tile: query qq's HQ
+// Scores of the queries in one 32-column pass of a group tile: query qq's HQ
 // head columns, ReLU, weighted sum with its w * scale, times the key scale.
 // (HQ a multiple of 4: the weights are read 4 at a time, sWg being 16-byte
 // aligned, and the even and odd heads are summed in the two halves of a packed
 // f32x2 FMA, then added.)
-template <int HQ, int W = 32>
-__device__ __forceinline__ void group_scores(const IndexParams &p, const float (&v)[W],
+template <int HQ>
+__device__ __forceinline__ void group_scores(const IndexParams &p, const float (&v)[32],
                                              const float *sWg, const int32_t *sNg, int c0, int nqp,
                                              int q0, int64_t j, float sk, int lane)
 {
 #pragma unroll
-    for (int k2 = 0; k2 < W / HQ; ++k2) {
+    for (int k2 = 0; k2 < 32 / HQ; ++k2) {
         if (k2 >= nqp) break;
         const int qq = c0 / HQ + k2;
         const float *wq = sWg + qq * HQ;
