@@ -720,6 +720,68 @@ def run_prefill(csa, args, world, dev):
     return res
 
 
+def run_encoder(csa, args, world, dev):
+    """The encoder's 18 CSA2 layers over one chunk of 4,096 causal queries
+    after a 262,144-token prefix: three blocks of 1 Full + 5 Reuse at m = 2,
+    each block with its own cache (the chunk's tokens appended to all three)."""
+    from sparse_attention_decode_step_gb300 import schedule as S
+    base = ci.config(4)
+    P, nq, m = base.ctx_tokens[0], base.q_per_seq, base.m
+    if args.ctx or args.queries:                          # smaller profiling case
+        P, nq = args.ctx or P, args.queries or nq
+        assert P % m == 0 and nq % (base.group * m) == 0
+    name = f"encoder_m{m}_prefix{P}_q{nq}"
+    wls = [ci.Workload(f"{name}_block{b}", 1, [P], nq, m, rms_norm=True, seed=base.seed + 100 * b,
+                       group=base.group, q_per_seq=nq) for b in range(3)]
+    caches = []
+    for wl in wls:
+        cache = build_cache(csa, wl, dev, extra=nq // m + 8)
+        C, Z = ci.latent_rows(wl, 0, P, nq, dev)
+        key = ci.key_rows(wl, 0, P // m, nq // m, dev)
+        csa.quantize_append(cache, C[None].contiguous(), Z[None].contiguous(), key[None].contiguous(),
+                            seq=0)
+        caches.append(cache)
+    q_pos = [P + i for i in range(nq)]
+    qs = csa.Queries([0] * nq, q_pos, base.group, dev)
+    n_max = (P + nq) // m
+    wcap = 8192
+    plan = S.encoder_csa2_layers()
+    per_layer = []
+    for i, p in enumerate(plan):
+        wl = wls[p.cache]
+        qi, w, qa = ci.query_inputs(wl, nq, dev, layer=i)
+        per_layer.append(dict(q_idx=qi, w=w, q=qa, win=ci.window_rows(wl, 1, wcap, dev, layer=i),
+                              out=torch.empty(nq, wl.heads, 512, device=dev)))
+    counters = csa.new_counters(dev)
+    chunk = S.EncoderChunk(csa, caches, qs, per_layer, k=base.k, n_win=base.n_win, max_n=n_max,
+                           counters=counters)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fns = list(chunk.layers)                              # one phase per layer
+    clocks = Clocks(torch.cuda.current_device()).__enter__()
+    sec, ph = timed_graphs(fns, args.steps, args.warmup, flush)
+    clocks.__exit__(None, None, None)
+    assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
+    _hbm, bf16, src = peaks()
+    reuse = [ph[i] for i, p in enumerate(plan) if p.mode == S.REUSE]
+    attn_flops = nq * 4 * base.heads * 512 * (base.k + base.n_win)   # one layer's attention
+    achieved = attn_flops * len(reuse) / sum(reuse) / 1e12
+    roof = {"kernel": "attn_tc_kernel (the 15 Reuse layers: attention alone)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": round(bf16, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / bf16, 4), "peak_source": src, "traffic": None,
+            "algorithmic_flops_per_launch": attn_flops}
+    phases = {}
+    for b in range(3):
+        lay = [i for i, p in enumerate(plan) if p.cache == b]
+        phases[f"block{b + 1}_full"] = ph[lay[0]]
+        phases[f"block{b + 1}_reuse_x5"] = float(sum(ph[i] for i in lay[1:]))
+    wl0 = wls[0]
+    wl0.name = name
+    return _line("encoder", wl0, args, world, nq * len(plan) / sec, "queries*layers/s", sec * 1e3,
+                 phases, roof, clocks,
+                 {"queries": nq, "prefix_tokens": P, "m": m, "group": base.group, "k": base.k,
+                  "heads": base.heads, "layers": "3 x (1 Full + 5 Reuse), three caches"})
+
+
 def run_schedule(csa, args, world, dev):
     """The 20-layer decoder (1 Full + 4 Reindex + 15 Reuse) over 64 sequences
     with log-uniform contexts in [4,096, 1,048,576], one query each."""
@@ -814,17 +876,20 @@ def main():
     ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
     ap.add_argument("--ctx", type=int, default=0,
                     help="profiling case: cached tokens per sequence instead of 65,535 "
-                         "(prefill: prefix tokens instead of 262,144)")
+                         "(prefill, encoder: prefix tokens instead of 262,144)")
     ap.add_argument("--queries", type=int, default=0,
-                    help="profiling case, prefill: queries instead of 4,096 (a multiple of 64)")
+                    help="profiling case, prefill / encoder: queries instead of 4,096 (a multiple "
+                         "of 64)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling case: skip the e2e and CPU-baseline legs")
     ap.add_argument("--d-idx", type=int, default=128, choices=[64, 128],
                     help="indexer key width of the decode_full workload (64: the 890 B/token layout)")
     ap.add_argument("--workload", default="decode_full",
-                    choices=["decode_full", "reindex", "prefill", "schedule"],
+                    choices=["decode_full", "reindex", "prefill", "encoder", "schedule"],
                     help="decode_full (default): 32 x 64K Full-mode decode step; reindex: Reindex "
-                         "layer at 1M; prefill: m = 2 encoder chunk; schedule: 20-layer decoder")
+                         "layer at 1M; prefill: m = 2 encoder chunk, one Full + five Reuse layers; "
+                         "encoder: the same chunk through the encoder's 18 CSA2 layers (three "
+                         "caches); schedule: 20-layer decoder")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -842,7 +907,8 @@ def main():
     else:
         import sparse_attention_decode_step_gb300 as csa
         dev = torch.device("cuda", torch.cuda.current_device())
-        run = {"reindex": run_reindex, "prefill": run_prefill, "schedule": run_schedule}
+        run = {"reindex": run_reindex, "prefill": run_prefill, "encoder": run_encoder,
+               "schedule": run_schedule}
         res = run[args.workload](csa, args, world, dev)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -102,3 +102,49 @@ class DecoderStep:
     def __call__(self):
         for layer in self.layers:
             layer()
+
+
+def encoder_csa2_layers():
+    """The encoder's CSA2 layers (3..20) in order: three blocks of 1 Full +
+    5 Reuse at m = 2, block b reading main-KV cache b."""
+    return [p for p in encoder_schedule() if p.mode != SWA]
+
+
+class EncoderChunk:
+    """Runs the encoder's 18 CSA2 layers over one chunk of prompt queries
+    through csa2_layer_step.
+
+    [Notes] section 2: each Full layer keeps its own compressed cache (here
+    caches[0..2], m = 2, one per block, the chunk's own tokens already
+    appended) and its five Reuse layers take its index list with their own
+    queries and windows.  per_layer[i] holds the inputs of CSA2 layer i (the
+    encoder's layer i + 3): q_idx and w (Full layers only), q, win, out and
+    an optional lse.  The two pure sliding-window layers in front (1 and 2)
+    are not part of this path.  One workspace serves every layer in turn."""
+
+    def __init__(self, csa, caches, qs, per_layer, *, k, n_win, max_n, sm_scale=1.0,
+                 counters=None):
+        import torch
+        self.plan = encoder_csa2_layers()
+        dev = per_layer[0]["q"].device
+        nq = qs.nq
+        n_blocks = 1 + max(p.cache for p in self.plan)
+        assert len(caches) == n_blocks and len(per_layer) == len(self.plan)
+        self.idx = [torch.zeros(nq, k, dtype=torch.int32, device=dev) for _ in range(n_blocks)]
+        self.cnt = [torch.zeros(nq, dtype=torch.int32, device=dev) for _ in range(n_blocks)]
+        ws = None
+        self.layers = []
+        for p, L in zip(self.plan, per_layer):
+            full = p.mode == FULL
+            layer = csa.Layer(csa.FULL if full else csa.REUSE, caches[p.cache], qs, k=k,
+                              q=L["q"], win=L["win"], n_win=n_win, out=L["out"],
+                              idx=self.idx[p.cache], cnt=self.cnt[p.cache],
+                              q_idx=L.get("q_idx") if full else None,
+                              w=L.get("w") if full else None, max_n=max_n, lse=L.get("lse"),
+                              sm_scale=sm_scale, counters=counters, ws=ws)
+            ws = layer.ws
+            self.layers.append(layer)
+
+    def __call__(self):
+        for layer in self.layers:
+            layer()

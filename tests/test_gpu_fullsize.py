@@ -251,3 +251,44 @@ def test_decoder_schedule_20_layers_mixed_lengths():
             if p.layer in (1, 4, 5, 20):
                 check_attention(wl, b, q_pos[b], sel[src], Ly["q"][b], Ly["win"], wcap,
                                 _np(Ly["out"][b]))
+
+
+def test_encoder_chunk_18_layers_three_caches():
+    """The encoder's 18 CSA2 layers (three blocks of 1 Full + 5 Reuse at m = 2)
+    over one chunk of 64 causal queries after a 16,000-token prefix, each block
+    with its own cache; exact-integer indexer inputs and exactly compressible
+    latents, as in the prefill test."""
+    P, nq = 16000, 64
+    wls = [ci.Workload(f"enc{b}", 1, [P], nq, 2, exact=True, grid=True, equal_z=True,
+                       seed=1100 + b, group=32, q_per_seq=nq) for b in range(3)]
+    caches = [build(wl, nq) for wl in wls]
+    q_pos = [P + i for i in range(nq)]
+    qs = csa.Queries([0] * nq, q_pos, 32, DEV)
+    wcap = 512
+    n_max = (P + nq) // 2
+    plan = S.encoder_csa2_layers()
+    per_layer = []
+    for i, p in enumerate(plan):
+        wl = wls[p.cache]
+        qi, w, qa = ci.query_inputs(wl, nq, DEV, layer=i)
+        per_layer.append(dict(q_idx=qi, w=w, q=qa, win=ci.window_rows(wl, 1, wcap, DEV, layer=i),
+                              out=torch.zeros(nq, wl.heads, 512, device=DEV)))
+    counters = csa.new_counters()
+    chunk = S.EncoderChunk(csa, caches, qs, per_layer, k=wls[0].k, n_win=wls[0].n_win,
+                           max_n=n_max, counters=counters)
+    chunk()
+    torch.cuda.synchronize()
+    assert _np(counters).tolist() == [0, 0, 0, 0]
+    for b in range(3):
+        wl = wls[b]
+        k8, ks = oracle_keys(wl, 0, n_max)
+        lay = [i for i, p in enumerate(plan) if p.cache == b]
+        full = per_layer[lay[0]]
+        for i in (0, 37, 63):
+            n = (q_pos[i] + 1) // 2
+            sc = O.scores_full(k8, ks, _np(full["q_idx"][i]), _np(full["w"][i]), 0, n)
+            ref = O.topk(sc, wl.k)
+            assert int(chunk.cnt[b][i]) == wl.k and np.array_equal(_np(chunk.idx[b][i]), ref), (b, i)
+            for j in (lay[0], lay[2], lay[5]):           # the Full layer and two Reuse layers
+                Ly = per_layer[j]
+                check_attention(wl, 0, q_pos[i], ref, Ly["q"][i], Ly["win"], wcap, _np(Ly["out"][i]))

@@ -45,6 +45,18 @@ def test_encoder_blocks():
         assert all(p.m == 2 and p.cache == b for p in blk)
 
 
+def test_encoder_csa2_layers_for_the_chunk_driver():
+    # the 18 layers EncoderChunk runs: blocks of 1 Full + 5 Reuse, block b on cache b,
+    # every Reuse layer fed by its own block's Full layer
+    plan = S.encoder_csa2_layers()
+    assert [p.layer for p in plan] == list(range(3, 21))
+    for b in range(3):
+        blk = plan[6 * b:6 * b + 6]
+        assert [p.mode for p in blk] == [S.FULL] + [S.REUSE] * 5
+        assert {p.cache for p in blk} == {b} and {p.m for p in blk} == {2}
+        assert all(p.source == blk[0].layer for p in blk[1:])
+
+
 def test_entries_per_token_and_kv_accounting():
     # three m = 2 encoder caches + one m = 1 decoder cache = 2.5 entries per token;
     # at 288 + 64 + 4 B per entry that is the pages' 890 B/token
