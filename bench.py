@@ -307,6 +307,12 @@ def run_csa2(args, rank, world):
 
     t_index = timed_call(ph_index)
     t_attn = timed_call(ph_attn)
+    # the append variant whose indexer keys are projected from the stored
+    # entries (random-init bf16 W_IK), the same 32 new tokens
+    g = torch.Generator(device=dev).manual_seed(7)
+    w_ik = (torch.randn(512, wl.d_idx, generator=g, device=dev) / 16).to(torch.bfloat16)
+    t_proj = timed_call(lambda: csa.quantize_append_project(cache, stage["C"], None, w_ik,
+                                                            counters=counters))
 
     # ---- roofline of the dominant kernel (Full-mode indexer)
     hbm, bf16, src = peaks()
@@ -339,6 +345,9 @@ def run_csa2(args, rank, world):
                           "bf16_frac": round(attn_flops / t_attn / 1e12 / bf16, 4)},
         "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
+        "append_project": {"entries": B, "launch_us": round(t_proj * 1e6, 2),
+                           "note": "append with keys projected from the stored entries (not "
+                                   "part of the timed step)"},
     }
     if rank == 0 and not args.quick:
         res["cpu_baseline"] = cpu_baseline(wl, cache, win, inputs[args.warmup], T0 + args.warmup)
@@ -717,6 +726,26 @@ def run_prefill(csa, args, world, dev):
                 roof, clocks, {"queries": nq, "prefix_tokens": P, "m": m, "group": wl.group,
                                "k": wl.k, "heads": wl.heads, "layers": "1 Full + 5 Reuse"})
     res["attn_bf16_frac"] = round(attn_flops / ph[2] / 1e12 / bf16, 4)
+    # the chunk's append with keys projected from the stored entries (random-init
+    # bf16 W_IK): nq / m entries, re-appended at the same rows each time
+    g = torch.Generator(device=dev).manual_seed(7)
+    w_ik = (torch.randn(512, wl.d_idx, generator=g, device=dev) / 16).to(torch.bfloat16)
+    len0 = cache.seq_len.clone() - nq // m
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for s_ in range(22):
+        flush.fill_(s_ & 0xFF)
+        cache.seq_len.copy_(len0)
+        ea.record()
+        csa.quantize_append_project(cache, C[None].contiguous(), Z[None].contiguous(), w_ik,
+                                    counters=counters, seq=0)
+        eb.record()
+        torch.cuda.synchronize()
+        if s_ >= 2:
+            ts.append(ea.elapsed_time(eb) / 1e3)
+    res["append_project"] = {"entries": nq // m, "launch_us": round(sum(ts) / len(ts) * 1e6, 2),
+                             "note": "append with keys projected from the stored entries (not "
+                                     "part of the timed step)"}
     return res
 
 

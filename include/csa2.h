@@ -131,6 +131,21 @@ csa2_status csa2_quantize_append(const csa2_cache *cache, const float *C, const 
                                  const float *key, int32_t n_tok, uint32_t *counters,
                                  void *stream);
 
+/* The same append with the indexer key projected from the stored entry
+ * instead of passed in ([Notes] section 1: the indexer key is a linear
+ * projection of the main KV; this library's reading: of the dequantised FP4
+ * entry, so that every key can be rebuilt from the cache alone):
+ *   key[b][e][d] = sum_c value(entry)[c] * w_ik[c][d], then FP8-encoded as in
+ *   csa2_quantize_append; the sum runs in fp32 over c = 0..511 in order.
+ *   w_ik [512][d_idx] bf16 (bit patterns), row c = latent channel c, device
+ *   memory, 16-byte aligned, owned by the caller and only read.
+ * Two launches (the appends, then the sequence-length update); the first
+ * stages w_ik (64 or 128 KB) in shared memory once per CTA.  Same status and
+ * counters as csa2_quantize_append. */
+csa2_status csa2_quantize_append_project(const csa2_cache *cache, const float *C,
+                                         const float *Z, const uint16_t *w_ik, int32_t n_tok,
+                                         uint32_t *counters, void *stream);
+
 /* ---- 2. Full-mode indexer -------------------------------------------------
  * scores[i][j] = sum_h w[i][h] * ReLU(q_h . k_j) for the visible entries
  * j < N_i = floor((q_pos[i]+1)/m) of query i ([Notes] section 2: a Full

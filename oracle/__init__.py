@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.or_compress_block.argtypes = [vp, vp, i32, vp]
             L.or_append.restype = i64
             L.or_append.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.or_append_project.restype = i64
+            L.or_append_project.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.or_scores_full.restype = None
             L.or_scores_full.argtypes = [vp, vp, i32, i32, vp, vp, i64, i64, vp]
             L.or_scores_at.restype = None
@@ -203,6 +205,27 @@ def append(C, Z, key, m):
     nsat = lib().or_append(B, n_tok, m, d_idx, _p(C), _p(Zc), _p(key), _p(codes), _p(scales),
                            _p(kidx), _p(ksc), _p(x))
     return codes, scales, kidx, ksc, x, int(nsat)
+
+
+def append_project(C, Z, w_ik, m):
+    """Append whose indexer key is the dequantised entry times W_IK.
+    C, Z: [B][n_tok][512] fp32; w_ik: [512][d_idx] bf16 bit patterns (uint16).
+    Returns codes, scales, kidx, kscale as append() does, the fp64 keys before
+    FP8 encoding [B*ne][d_idx], and the number of saturated groups."""
+    C = _c(C, np.float32)
+    B, n_tok, _ = C.shape
+    Zc = _c(Z, np.float32) if m > 1 else None
+    w_ik = _c(w_ik, np.uint16)
+    d_idx = w_ik.shape[1]
+    ne = n_tok // m
+    codes = np.zeros((B * ne, D // 2), np.uint8)
+    scales = np.zeros((B * ne, D // 16), np.uint8)
+    kidx = np.zeros((B * ne, d_idx), np.uint8)
+    ksc = np.zeros(B * ne, np.float32)
+    k = np.zeros((B * ne, d_idx), np.float64)
+    nsat = lib().or_append_project(B, n_tok, m, d_idx, _p(C), _p(Zc), _p(w_ik), _p(codes),
+                                   _p(scales), _p(kidx), _p(ksc), _p(k))
+    return codes, scales, kidx, ksc, k, int(nsat)
 
 
 # ----------------------------------------------------------------- indexer

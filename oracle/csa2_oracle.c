@@ -251,6 +251,40 @@ int64_t or_append(int B, int n_tok, int m, int d_idx, const float *C, const floa
     return nsat;
 }
 
+/* Append with the indexer key projected from the stored entry: the key of an
+ * entry is the dequantised FP4 latent times W_IK ([Notes] section 1: the
+ * indexer key is a linear projection of the main KV; this library's reading:
+ * of the dequantised FP4 entry, so that the key can be rebuilt from the
+ * persisted cache alone), then FP8-encoded like a caller-given key.
+ * w_ik: bf16 bit patterns [512][d_idx], row c = latent channel c.  Other
+ * arguments and outputs as in or_append (no key input). */
+int64_t or_append_project(int B, int n_tok, int m, int d_idx, const float *C, const float *Z,
+                          const uint16_t *w_ik, uint8_t *codes, uint8_t *scales, uint8_t *kidx,
+                          float *kscale, double *kout)
+{
+    int ne = n_tok / m;
+    int64_t nsat = 0;
+#pragma omp parallel for reduction(+ : nsat) schedule(static)
+    for (int64_t r = 0; r < (int64_t)B * ne; ++r) {
+        int64_t b = r / ne, e = r % ne;
+        double x[OR_D], v[OR_D], k[1024];
+        const float *cb = C + (b * n_tok + e * m) * OR_D;
+        const float *zb = (m > 1) ? Z + (b * n_tok + e * m) * OR_D : NULL;
+        or_compress_block(cb, zb, m, x);
+        uint8_t *cr = codes + r * (OR_D / 2), *sr = scales + r * OR_NGROUP;
+        nsat += or_fp4_encode_entry(x, cr, sr);
+        or_fp4_decode_entry(cr, sr, v);
+        for (int d = 0; d < d_idx; ++d) {
+            double acc = 0.0;
+            for (int c = 0; c < OR_D; ++c) acc += v[c] * or_bf16_value(w_ik[c * d_idx + d]);
+            k[d] = acc;
+        }
+        if (kout) memcpy(kout + r * d_idx, k, sizeof(double) * d_idx);
+        kscale[r] = (float)or_fp8_encode_vec(k, d_idx, kidx + r * d_idx);
+    }
+    return nsat;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Indexer scores  [Notes] sections 2-3, [Deep read] section 03               */
 /* ------------------------------------------------------------------------ */

@@ -26,7 +26,7 @@ _lib = None
 _STATUS = {0: "ok", -1: "invalid argument", -2: "pointer not 16-byte aligned",
            -3: "workspace or output too small", -4: "shape not supported", -5: "CUDA error"}
 
-EXPORTS = ["csa2_quantize_append", "csa2_index_full", "csa2_index_reindex", "csa2_topk",
+EXPORTS = ["csa2_quantize_append", "csa2_quantize_append_project", "csa2_index_full", "csa2_index_reindex", "csa2_topk",
            "csa2_pool_select", "csa2_sparse_attn", "csa2_layer_step", "csa2_index_workspace_size",
            "csa2_topk_workspace_size", "csa2_attn_workspace_size", "csa2_layer_workspace_size",
            "csa2_status_string", "csa2_launch_count", "csa2_topk_noalloc",
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
             sig = {
                 "csa2_quantize_append": [vp, vp, vp, vp, i32, vp, vp],
+                "csa2_quantize_append_project": [vp, vp, vp, vp, i32, vp, vp],
                 "csa2_index_full": [vp, vp, vp, vp, i32, i64, vp, i64, vp, i64, vp, vp, sz, vp, vp],
                 "csa2_index_reindex": [vp, vp, vp, vp, i32, vp, vp, i32, vp, i64, vp, vp, sz, vp,
                                        vp],
@@ -192,6 +193,20 @@ def quantize_append(cache: Cache, C, Z, key, counters=None, seq=None):
     cs = cache.struct(seq)
     _check(lib().csa2_quantize_append(ctypes.byref(cs), _ptr(C), _ptr(Z), _ptr(key), n_tok,
                                       _ptr(counters), _stream()), "csa2_quantize_append")
+
+
+def quantize_append_project(cache: Cache, C, Z, w_ik, counters=None, seq=None):
+    """Appends C.shape[1] tokens to every sequence (or only to sequence `seq`),
+    each entry's indexer key projected from the stored entry by w_ik, a bf16
+    tensor [512][d_idx]."""
+    if w_ik.dtype != torch.bfloat16 or tuple(w_ik.shape) != (512, cache.d_idx):
+        raise CsaError(f"w_ik must be bf16 [512][{cache.d_idx}], got {w_ik.dtype} {tuple(w_ik.shape)}")
+    n_tok = int(C.shape[1])
+    cs = cache.struct(seq)
+    _check(lib().csa2_quantize_append_project(ctypes.byref(cs), _ptr(C), _ptr(Z),
+                                              _ptr(w_ik.contiguous()), n_tok, _ptr(counters),
+                                              _stream()),
+           "csa2_quantize_append_project")
 
 
 def index_workspace_size(nq, group, h_idx, d_idx) -> int:

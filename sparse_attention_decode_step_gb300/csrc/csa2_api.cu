@@ -185,6 +185,20 @@ csa2_status csa2_quantize_append(const csa2_cache *cache, const float *C, const 
                                      static_cast<cudaStream_t>(stream)));
 }
 
+csa2_status csa2_quantize_append_project(const csa2_cache *cache, const float *C,
+                                         const float *Z, const uint16_t *w_ik, int32_t n_tok,
+                                         uint32_t *counters, void *stream)
+{
+    csa2_status s = check_cache(cache, true);
+    if (s != CSA2_OK) return s;
+    CSA2_REQUIRE(n_tok > 0 && n_tok % cache->m == 0, CSA2_ERR_INVALID_ARG);
+    CSA2_REQUIRE(C && w_ik && (cache->m == 1 || Z), CSA2_ERR_INVALID_ARG);
+    CSA2_REQUIRE(al16(C) && al16(w_ik) && (Z == nullptr || al16(Z)), CSA2_ERR_ALIGN);
+    CSA2_REQUIRE(counters == nullptr || al16(counters), CSA2_ERR_ALIGN);
+    return cuda_status(launch_append_project(*cache, C, Z, w_ik, n_tok, counters,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 csa2_status csa2_index_full(const csa2_cache *cache, const csa2_queries *queries,
                             const float *q_idx, const float *w, int32_t h_idx, int64_t max_n,
                             float *scores, int64_t ld_scores, float *blockmax,

@@ -55,6 +55,9 @@ cudaError_t make_tmap_rows_u8(CUtensorMap *map, const void *base, int64_t rows, 
 // ---- append
 cudaError_t launch_append(const csa2_cache &c, const float *C, const float *Z, const float *key,
                           int n_tok, uint32_t *counters, cudaStream_t st);
+cudaError_t launch_append_project(const csa2_cache &c, const float *C, const float *Z,
+                                  const uint16_t *w_ik, int n_tok, uint32_t *counters,
+                                  cudaStream_t st);
 
 // ---- indexer
 size_t index_workspace_bytes(int nq, int group, int h_idx, int d_idx);

@@ -75,6 +75,12 @@ def test_append_rejects_bad_arguments_on_host():
                                   None) == -2
     # NULL cache
     assert L.csa2_quantize_append(None, ok_ptr, None, ok_ptr, 1, None, None) == -1
+    # the projecting append: w_ik required and 16-byte aligned, same cache checks
+    assert L.csa2_quantize_append_project(ctypes.byref(c), ok_ptr, None, None, 1, None, None) == -1
+    assert L.csa2_quantize_append_project(ctypes.byref(c), ok_ptr, None, ctypes.c_void_p(4100), 1,
+                                          None, None) == -2
+    assert L.csa2_quantize_append_project(ctypes.byref(c3), ok_ptr, None, ok_ptr, 1, None,
+                                          None) == -4
     # capacity must be a multiple of 8
     c4 = _cache(cap=60)
     assert L.csa2_quantize_append(ctypes.byref(c4), ok_ptr, None, ok_ptr, 1, None, None) == -1

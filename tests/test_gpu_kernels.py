@@ -107,6 +107,75 @@ def test_append_m2_random_differs_only_at_rounding_boundaries():
         assert abs(x[r, c] - mid) <= 1e-5 * abs(mid), (r, c, x[r, c], dg[r, c], do[r, c])
 
 
+def _bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("d_idx,m", [(128, 1), (64, 1), (128, 2)])
+def test_append_project_exact_inputs_bit_exact(d_idx, m):
+    # integer latents in [-6, 6] with a 6 in every group (all scales 1.0; at m = 2
+    # equal Z makes each entry the exact mean of its two tokens) and W_IK entries
+    # k / 64: the projected keys are exact in fp32, so every byte matches.
+    # 4 sequences x 8 tokens (decode-sized) and one sequence of 3,000 tokens
+    # (many entries per warp)
+    g = torch.Generator().manual_seed(44)
+    w = _bf16(torch.randint(-64, 65, (512, d_idx), generator=g) / 64.0)
+    wbits = w.view(torch.int16).numpy().view(np.uint16)
+    for B, n_tok in ((4, 8), (1, 3000)):
+        C = torch.randint(-6, 7, (B, n_tok, 512), generator=g).float()
+        C[..., ::16] = 6.0
+        Z = None
+        if m == 2:
+            Z = torch.randn(B, n_tok // 2, 1, 512, generator=g).expand(B, n_tok // 2, 2, 512)
+            Z = Z.reshape(B, n_tok, 512).contiguous()
+        ne = n_tok // m
+        cache = csa.Cache([ne + 8] * B, d_idx, m, DEV)
+        cnt = csa.new_counters()
+        csa.quantize_append_project(cache, C.to(DEV), None if Z is None else Z.to(DEV), w.to(DEV),
+                                    counters=cnt)
+        torch.cuda.synchronize()
+        assert _np(cache.seq_len).tolist() == [ne] * B and _np(cnt).tolist() == [0, 0, 0, 0]
+        codes, scales, kidx, ksc, _k, _ = O.append_project(C.numpy(),
+                                                           None if Z is None else Z.numpy(), wbits, m)
+        for b in range(B):
+            r0, sl = cache.base_host[b], slice(b * ne, (b + 1) * ne)
+            assert np.array_equal(_np(cache.codes[r0:r0 + ne]), codes[sl])
+            assert np.array_equal(_np(cache.scales[r0:r0 + ne]), scales[sl])
+            assert np.array_equal(_np(cache.kidx[r0:r0 + ne]), kidx[sl])
+            assert np.array_equal(_np(cache.kscale[r0:r0 + ne]), ksc[sl])
+
+
+def test_append_project_random_differs_only_at_rounding_boundaries():
+    # random latents and W_IK (m = 1: the FP4 entries are bit-exact for any
+    # input); each key byte matches the oracle unless the fp64 key sits on the
+    # E4M3 rounding midpoint that the fp32 sum fell across
+    g = torch.Generator().manual_seed(45)
+    B, n_tok, d_idx = 2, 512, 128
+    C = torch.randn(B, n_tok, 512, generator=g)
+    w = _bf16(torch.randn(512, d_idx, generator=g) / 16.0)
+    cache = csa.Cache([n_tok + 8] * B, d_idx, 1, DEV)
+    csa.quantize_append_project(cache, C.to(DEV), None, w.to(DEV))
+    torch.cuda.synchronize()
+    wbits = w.view(torch.int16).numpy().view(np.uint16)
+    codes, scales, kidx, ksc, k, _ = O.append_project(C.numpy(), None, wbits, 1)
+    ne = n_tok
+    gc = np.concatenate([_np(cache.codes[cache.base_host[b]:cache.base_host[b] + ne]) for b in range(B)])
+    gs = np.concatenate([_np(cache.scales[cache.base_host[b]:cache.base_host[b] + ne]) for b in range(B)])
+    gk = np.concatenate([_np(cache.kidx[cache.base_host[b]:cache.base_host[b] + ne]) for b in range(B)])
+    gks = np.concatenate([_np(cache.kscale[cache.base_host[b]:cache.base_host[b] + ne]) for b in range(B)])
+    assert np.array_equal(gc, codes) and np.array_equal(gs, scales)
+    rows = np.arange(B * ne)
+    assert np.array_equal(gks[rows], ksc[rows])   # no amax on a power-of-two edge here
+    tab = O.e4m3_values(np.arange(256))
+    y = k[rows] / ksc[rows, None]
+    diff = np.argwhere(gk[rows] != kidx[rows])
+    assert len(diff) <= 1e-3 * y.size
+    for r, c in diff:
+        a, b_ = tab[gk[rows][r, c]], tab[kidx[rows][r, c]]
+        mid = 0.5 * (a + b_)
+        assert abs(y[r, c] - mid) <= 1e-5 * max(1.0, abs(mid)), (r, c, y[r, c], a, b_)
+
+
 def test_append_saturation_and_capacity_counters():
     cache = csa.Cache([16], 128, 1, DEV)
     C = torch.zeros(1, 8, 512)

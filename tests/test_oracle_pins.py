@@ -245,6 +245,70 @@ def test_append_batch_layout():
             assert np.array_equal(k8[0], kidx[r]) and ks[0] == ksc[r]
 
 
+# --------------------------------------------------------------- projected indexer key
+def _bf16_bits(x):
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_values(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _dequant_entries(codes, scales):
+    # decode with the golden E2M1 table and the library's E4M3 decode
+    e2m1 = {int(c): float(v) for c, v in (l.split() for l in open(golden("e2m1_values.txt"))
+                                          if l.strip() and not l.startswith("#"))}
+    nib = np.stack([codes & 15, codes >> 4], -1).reshape(codes.shape[0], 512)
+    vals = np.vectorize(e2m1.get)(nib).astype(np.float64)
+    return vals * np.repeat(_torch_e4m3_table()[scales.astype(np.int64)], 16, axis=1)
+
+
+def test_append_project_is_stored_entry_times_w():
+    # key = (dequantised stored entry) @ W_IK, then the FP8 encoding of a given key
+    rng = np.random.default_rng(41)
+    for m, d in ((1, 128), (2, 64)):
+        C = rng.normal(size=(2, 4 * m, 512)).astype(np.float32)
+        Z = rng.normal(size=(2, 4 * m, 512)).astype(np.float32)
+        wbits = _bf16_bits(rng.normal(size=(512, d)) / 16)
+        codes, scales, kidx, ksc, k, nsat = O.append_project(C, Z, wbits, m)
+        c2, s2, _k, _s, _x, _ = O.append(C, Z, np.zeros((2, 4, d), np.float32), m)
+        assert np.array_equal(codes, c2) and np.array_equal(scales, s2) and nsat == 0
+        want = _dequant_entries(codes, scales) @ _bf16_values(wbits)      # numpy matmul
+        assert np.allclose(k, want, rtol=1e-12, atol=1e-12)
+        # FP8 step: the library's round-to-nearest-even E4M3 of k / scale
+        lib8 = torch.from_numpy(k / ksc[:, None].astype(np.float64)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(kidx, lib8)
+        assert all(ks == O.fp8_pow2_scale(np.abs(kk).max()) for kk, ks in zip(k, ksc))
+
+
+def test_append_project_identity_rows_give_the_entry():
+    # W = [I; 0]: the key is the first d channels of the stored entry (pins the
+    # orientation: row c of W_IK multiplies latent channel c)
+    rng = np.random.default_rng(42)
+    C = rng.normal(size=(1, 3, 512)).astype(np.float32)
+    w = np.zeros((512, 128), np.float32)
+    w[np.arange(128), np.arange(128)] = 1.0
+    codes, scales, _kidx, _ksc, k, _ = O.append_project(C, None, _bf16_bits(w), 1)
+    assert np.array_equal(k, _dequant_entries(codes, scales)[:, :128])
+
+
+def test_append_project_exact_inputs_are_exact():
+    # integer latents in [-6, 6] with a 6 in every 16-channel group: every scale
+    # is 1.0, stored values are multiples of 1/2, and with W_IK entries k / 64
+    # every product and partial sum is a multiple of 1/128 below 2^12 -- exact
+    # in fp32 in any order, so a fp32 kernel and this fp64 oracle agree bit for bit
+    rng = np.random.default_rng(43)
+    C = rng.integers(-6, 7, size=(1, 5, 512)).astype(np.float32)
+    C[..., ::16] = 6.0
+    w = rng.integers(-64, 65, size=(512, 128)) / 64.0
+    codes, scales, kidx, ksc, k, _ = O.append_project(C, None, _bf16_bits(w), 1)
+    assert (scales == 0x38).all()
+    assert np.array_equal(k * 128, np.round(k * 128)) and np.abs(k).max() < 4096
+    assert np.array_equal(k.astype(np.float32).astype(np.float64), k)
+
+
 # --------------------------------------------------------------- scores
 def _dequant_fp8(b, s):
     return _torch_e4m3_table()[b.astype(np.int64)] * s[..., None]
