@@ -48,11 +48,14 @@ def build(force: bool = False) -> str:
 
 
 def lib() -> ctypes.CDLL:
+    """The compiled oracle.  CSA2_ORACLE_LIB, when set, names another build of
+    this source to load instead (the mutation test loads copies with a
+    planted mistake that way)."""
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_LIB_PATH)
+            path = os.environ.get("CSA2_ORACLE_LIB") or build()
+            L = ctypes.CDLL(path)
             dbl, i32, i64, vp = ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
             L.or_e2m1_value.restype = dbl
             L.or_e2m1_value.argtypes = [i32]
