@@ -42,14 +42,20 @@ import csa2_inputs as ci  # noqa: E402
 METRIC = "CSA2 decode queries/s/layer at 64K-1M ctx; HBM GB/s & FP8 util vs GB300 peak"
 UNIT = "queries/s/layer"
 L2_FLUSH_BYTES = 512 << 20
-# algorithmic bytes of the Full-mode indexer per visible entry: 128 B FP8 key +
-# 4 B key scale read, 4 B score written
-IDX_BYTES_PER_ENTRY = 128 + 4 + 4     # FP8 key (d_idx = 128) + key scale + score
+DTYPE = ("fp8 e4m3 indexer MMA (fp32 accumulate); f16 attention MMA operands (FP4 latents "
+         "dequantised exactly to f16, bf16 q and window converted to f16, P in f16), fp32 "
+         "accumulate and softmax")
+# DRAM bytes (read + write) per visible entry of the decode indexer kernel,
+# index_main_kernel, from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# on the 32 x 32,768 decode case; the capture's provenance is stated with the
+# measurement notes.  None once the kernel has changed since that capture.
+INDEX_DRAM_BYTES_PER_ENTRY = 137.0
 
 
 def idx_bytes_per_entry(d_idx):
-    return d_idx + 4 + 4
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "index_main_decode_b32_ctx32768.md")
+    """Algorithmic bytes of the indexer per scored entry: the FP8 key and its
+    fp32 scale (the score write is not counted: it need not leave the chip)."""
+    return d_idx + 4
 
 
 def peaks():
@@ -61,65 +67,137 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def profiled_bytes_per_entry():
-    """DRAM bytes per visible entry of the indexer kernel (read + write), from
-    the committed ncu summary of a smaller case of the same kernel; None if
-    there is none."""
-    if not os.path.exists(PROFILE_SUMMARY):
-        return None
-    for line in open(PROFILE_SUMMARY):
-        if line.startswith("dram_bytes_per_visible_entry:"):
-            v = line.split(":", 1)[1].strip()
-            return None if v in ("", "null") else float(v)
-    return None
+class _Nvml:
+    """Read-only NVML queries through ctypes (the driver's libnvidia-ml), for
+    the device torch calls `index` (found by UUID, else by PCI bus id)."""
+    CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(index)
+        rc = -1
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            rc = self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h))
+        if rc != 0 and hasattr(props, "pci_bus_id"):
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError(f"no NVML handle for device {index} (rc {rc})")
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(clk)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        if self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(rs)) != 0:
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(self.h, ct.byref(rs))
+        names = [n for bit, n in self.REASONS.items() if rs.value & bit]
+        return float(clk.value), pw.value / 1000.0, names
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """SM clock, power and clock-event reasons sampled every 10 ms during the
+    timed region, in-process through NVML (read-only queries) on a background
+    thread; if NVML cannot be used, an nvidia-smi child process queries the
+    same device by UUID.  Errors are kept in the summary."""
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
+        self.samples, self.errors = [], []
+        self.max_mhz = None
+        self._stop = None
 
     def __enter__(self):
+        import threading
+        try:
+            nv = _Nvml(self.index)
+            self.max_mhz = nv.max_mhz
+            self._stop = threading.Event()
+
+            def loop():
+                while not self._stop.is_set():
+                    try:
+                        s_ = nv.sample()
+                        if s_ is not None:
+                            self.samples.append(s_)
+                    except Exception as e:   # keep sampling; record the first error
+                        if len(self.errors) < 3:
+                            self.errors.append(f"nvml sample: {e}")
+                    self._stop.wait(0.01)
+            self._thr = threading.Thread(target=loop, daemon=True)
+            self._thr.start()
+            self.proc = None
+        except Exception as e:
+            self.errors.append(f"nvml: {e}")
+            self._start_smi()
+        return self
+
+    def _start_smi(self):
+        try:
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+            dev = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            dev = str(self.index)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}",
-                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                ["nvidia-smi", "-i", dev,
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "10"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
+                stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        except OSError as e:
             self.proc = None
-        return self
+            self.errors.append(f"nvidia-smi: {e}")
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
+        if self._stop is not None:
+            self._stop.set()
+            self._thr.join(timeout=5)
+        if getattr(self, "proc", None) is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                out, err = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                out, err = self.proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.max_mhz = float(f[1])
+                    self.samples.append((float(f[0]), float(f[2]),
+                                         [n for n, v in zip(names, f[3:7]) if v.lower() == "active"]))
+                except (ValueError, IndexError):
+                    continue
+            if not self.samples and err:
+                self.errors.append("nvidia-smi: " + err.strip()[:200])
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
-            except (ValueError, IndexError):
-                continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [x[0] for x in self.samples]
+        pw = [x[1] for x in self.samples]
+        reasons = sorted({r for x in self.samples for r in x[2]})
+        res = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": len(sm),
+               "power_w_max": round(max(pw), 1) if pw else None,
+               "source": "nvml" if self._stop is not None else "nvidia-smi"}
+        if self.errors:
+            res["errors"] = self.errors
+        return res
 
 
 def job_time(local_seconds, world, device):
@@ -319,7 +397,7 @@ def run_csa2(args, rank, world):
     entries = B * (int(qs.q_pos[0]) + 1)                 # visible entries of those calls
     idx_bytes = entries * idx_bytes_per_entry(wl.d_idx)
     achieved = idx_bytes / t_index / 1e9
-    traffic = profiled_bytes_per_entry() if wl.d_idx == 128 else None
+    traffic = INDEX_DRAM_BYTES_PER_ENTRY if wl.d_idx == 128 else None
     roof = {"kernel": "index_main_kernel (+ index_prep_kernel; one csa2_index_full call)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_source": src,
@@ -332,7 +410,7 @@ def run_csa2(args, rank, world):
     res = {
         "metric": METRIC, "value": round(job_value(B * args.steps, world, total), 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (indexer MMA), fp4/bf16 -> fp32 (attention)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded counter-hash generator; N(0,1) latents scaled to norm sqrt(512))",
         "config": {"workload": wl.name, "batch": B, "ctx_tokens": T0 + 1, "m": wl.m,
                    "indexer_heads": wl.h_idx, "d_idx": wl.d_idx, "heads": wl.heads, "k": wl.k,
@@ -340,8 +418,17 @@ def run_csa2(args, rank, world):
                    "graph": "one CUDA graph replay per step", "parallelism": f"replicas x{world}"},
         "phases_us": {"append": round(ph[0] * 1e6, 2), "index_full": round(ph[1] * 1e6, 2),
                       "topk": round(ph[2] * 1e6, 2), "sparse_attn": round(ph[3] * 1e6, 2)},
-        "attn_roofline": {"bytes": attn_bytes, "flops": attn_flops, "launch_us": round(t_attn * 1e6, 2),
+        "attn_roofline": {"kernel": "attn_tc_kernel (one csa2_sparse_attn call)", "bound": "hbm",
+                          "achieved": round(attn_bytes / t_attn / 1e9, 1), "peak": hbm,
+                          "unit": "GB/s", "frac": round(attn_bytes / t_attn / 1e9 / hbm, 4),
+                          "peak_source": src, "traffic": None,
+                          "algorithmic_bytes_per_launch": attn_bytes,
+                          "launch_us": round(t_attn * 1e6, 2),
                           "hbm_frac": round(attn_bytes / t_attn / 1e9 / hbm, 4),
+                          "bf16": {"achieved": round(attn_flops / t_attn / 1e12, 1),
+                                   "peak": bf16, "unit": "TFLOP/s",
+                                   "frac": round(attn_flops / t_attn / 1e12 / bf16, 4),
+                                   "algorithmic_flops_per_launch": attn_flops},
                           "bf16_frac": round(attn_flops / t_attn / 1e12 / bf16, 4)},
         "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
@@ -593,7 +680,7 @@ def _line(name, wl, args, world, value, unit, ms, phases, roofline, clocks, extr
     res = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "fp8 (indexer MMA), fp4/bf16 -> fp32 (attention)",
+           "dtype": DTYPE,
            "data": "synthetic (seeded counter-hash generator)",
            "config": {"workload": wl.name, "l2": "flushed between steps (512 MB write)",
                       "graph": "one CUDA graph replay per step", "parallelism": f"replicas x{world}"},
@@ -652,7 +739,7 @@ def run_reindex(csa, args, world, dev):
     assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
     pn = int(pool_n.sum())
     hbm, _bf16, src = peaks()
-    ib = pn * IDX_BYTES_PER_ENTRY + B * 2048 * 4
+    ib = pn * idx_bytes_per_entry(wl.d_idx) + B * 2048 * 4
     roof = {"kernel": "index_main_kernel (Reindex, 8-row TMA boxes)", "bound": "hbm",
             "achieved": round(ib / ph[0] / 1e9, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(ib / ph[0] / 1e9 / hbm, 4), "peak_source": src, "traffic": None,
@@ -838,7 +925,7 @@ def run_schedule(csa, args, world, dev):
     clocks.__exit__(None, None, None)
     assert int(counters[csa.CNT_BAD_INPUT]) == 0 and int(counters[csa.CNT_TIMEOUT]) == 0, counters
     hbm, _bf16, src = peaks()
-    ib = sum(lens) * IDX_BYTES_PER_ENTRY
+    ib = sum(lens) * idx_bytes_per_entry(wl.d_idx)
     roof = {"kernel": "index_main_kernel (layer-1 Full scoring)", "bound": "hbm",
             "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None, "peak_source": src,
             "traffic": None, "algorithmic_bytes_full_layer": ib,
@@ -848,6 +935,28 @@ def run_schedule(csa, args, world, dev):
                  {"batch": B, "ctx_tokens": "log-uniform [4096, 1048576]",
                   "mean_ctx": int(sum(lens) / B), "layers": "1 Full + 4 Reindex + 15 Reuse",
                   "k": wl.k, "heads": wl.heads})
+
+
+def extra_workloads(args, world):
+    """The other configurations at their full sizes, each as in its own
+    --workload run but with fewer steps: Reindex decode over the candidate pool
+    at 1M context, the 20-layer decoder over 64 log-uniform contexts, and the
+    m = 2 prefill chunk (its FP8 scoring roofline).  Each entry keeps the
+    workload's value, ms_per_step, phase split, roofline and clock record."""
+    import sparse_attention_decode_step_gb300 as csa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sub = argparse.Namespace(**vars(args))
+    sub.steps, sub.warmup, sub.ctx, sub.queries = min(args.steps, 10), 3, 0, 0
+    out = {}
+    for key, fn in (("reindex_b8_1m", run_reindex), ("schedule20_b64", run_schedule),
+                    ("prefill_m2_q4096", run_prefill)):
+        torch.cuda.empty_cache()
+        r = fn(csa, sub, world, dev)
+        keep = ["value", "unit", "ms_per_step", "steps", "warmup", "phases_us", "roofline",
+                "clocks", "config", "attn_bf16_frac", "append_project"]
+        out[key] = {k_: r[k_] for k_ in keep if k_ in r}
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_reference(args, rank, world):
@@ -911,6 +1020,9 @@ def main():
                          "of 64)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling case: skip the e2e and CPU-baseline legs")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="decode_full: skip the Reindex 1M, 20-layer schedule and prefill "
+                         "workloads that the default run reports under `workloads`")
     ap.add_argument("--d-idx", type=int, default=128, choices=[64, 128],
                     help="indexer key width of the decode_full workload (64: the 890 B/token layout)")
     ap.add_argument("--workload", default="decode_full",
@@ -933,6 +1045,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.workload == "decode_full":
         res = run_csa2(args, rank, world)
+        if not args.quick and not args.no_extra:
+            res["workloads"] = extra_workloads(args, world)
     else:
         import sparse_attention_decode_step_gb300 as csa
         dev = torch.device("cuda", torch.cuda.current_device())

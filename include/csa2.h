@@ -139,9 +139,15 @@ csa2_status csa2_quantize_append(const csa2_cache *cache, const float *C, const 
  *   csa2_quantize_append; the sum runs in fp32 over c = 0..511 in order.
  *   w_ik [512][d_idx] bf16 (bit patterns), row c = latent channel c, device
  *   memory, 16-byte aligned, owned by the caller and only read.
- * Two launches (the appends, then the sequence-length update); the first
- * stages w_ik (64 or 128 KB) in shared memory once per CTA.  Same status and
- * counters as csa2_quantize_append. */
+ * One launch when n_tok / m <= 8 (decode: one CTA per sequence appends its
+ * entries and advances seq_len itself), two otherwise (the appends, then the
+ * sequence-length update); each CTA stages w_ik (64 or 128 KB) in shared
+ * memory.  Same status and counters as csa2_quantize_append.  If a CTA's wait
+ * for its copy of w_ik runs past its time limit (CSA2_CNT_TIMEOUT), the keys
+ * of its remaining entries are not written: in the one-launch form that
+ * sequence's seq_len is not advanced; in the two-launch form the entries are
+ * committed all the same and their keys are unspecified, so a cache that saw
+ * CSA2_CNT_TIMEOUT from this call must not be scored. */
 csa2_status csa2_quantize_append_project(const csa2_cache *cache, const float *C,
                                          const float *Z, const uint16_t *w_ik, int32_t n_tok,
                                          uint32_t *counters, void *stream);
@@ -236,9 +242,16 @@ csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const i
  *   out[i][h] = sum_r softmax_r(sm_scale * q[i][h] . v_r) v_r,
  *   lse[i][h] = log sum_r exp(sm_scale * q[i][h] . v_r)   (nullable).
  *   idx [nq][ld_idx] entry numbers < N_i (others are skipped and counted);
- *   q [nq][H][512] bf16 bits; H in {16, 32, 48, 64};
+ *   q [nq][H][512] bf16 bits; 1 <= H <= 64;
  *   win [batch][wcap][512] bf16 bits (NULL allowed when n_win == 0);
  *   out [nq][H][512] fp32; k_max >= every cnt[i].
+ * Arithmetic: the tensor-core products take f16 operands.  The dequantised
+ * FP4 values are exact in f16; q and the window rows are converted from bf16
+ * to f16, which is exact for magnitudes in [2^-14, 65504] (smaller ones become
+ * f16 subnormals with an absolute error below 2^-25; 65504 and above are
+ * outside the contract); the softmax weights P are stored as f16 (at most 256
+ * before normalisation, relative error 2^-11).  Logits, the softmax and every
+ * sum are fp32.
  * The attention needs no workspace (csa2_attn_workspace_size() is 0; the
  * argument may be NULL): a query's row tiles are divided over at most 8 CTAs
  * of one thread-block cluster, which merge on chip. */

@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(kProjThreads) append_project_kernel(
 {
     extern __shared__ __align__(16) uint8_t smem_proj[];
     __shared__ __align__(8) uint64_t bar_w;
+    __shared__ int s_timeout;             // a warp gave up waiting for W_IK
     const int d_idx = cache.d_idx;
     const uint32_t w_bytes = (uint32_t)CSA2_D * (uint32_t)d_idx * 2u;
     uint16_t *sW = reinterpret_cast<uint16_t *>(smem_proj);                   // [512][d_idx]
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kProjThreads) append_project_kernel(
     if (threadIdx.x == 0) {
         mbar_init(&bar_w, 1);
         fence_barrier_init();
+        s_timeout = 0;
     }
     __syncthreads();
     pdl_wait();
@@ -349,7 +351,10 @@ __global__ void __launch_bounds__(kProjThreads) append_project_kernel(
             // W_IK has landed (bounded wait; on expiry the key is not written)
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_w, 0, &no_abort));
             if (!ok) {
-                if (lane == 0) count_event(counters, CSA2_CNT_TIMEOUT);
+                if (lane == 0) {
+                    count_event(counters, CSA2_CNT_TIMEOUT);
+                    s_timeout = 1;
+                }
                 break;
             }
             w_ready = true;
@@ -360,7 +365,9 @@ __global__ void __launch_bounds__(kProjThreads) append_project_kernel(
     __syncthreads();
     // no copy of this CTA may still be landing when it exits (bounded)
     if (threadIdx.x == 0) mbar_wait(&bar_w, 0, &no_abort);
-    if (kFused && threadIdx.x == 0) {
+    // a sequence whose keys were not all written keeps its length (fused path;
+    // the two-launch path advances every sequence with room)
+    if (kFused && threadIdx.x == 0 && s_timeout == 0) {
         const int b = blockIdx.x;
         const int64_t room = cache.seq_base[b + 1] - cache.seq_base[b];
         const int64_t len = cache.seq_len[b];

@@ -465,3 +465,132 @@ def test_attention_more_queries_than_sms_single_split():
     cnts = rng.integers(0, 257, size=156).tolist()
     cnts[:3] = [0, 256, 1]
     _attn_case(64, 256, cnts, 32, 64, seed=35)
+
+
+# ---------------------------------------------------------------- peaky attention
+# The kernel keeps, per head, a reference max that moves only when a tile's
+# logit exceeds it by more than 8 (log2 units); the output accumulator is then
+# rescaled in tensor memory.  A query's tile range may be split over up to 8
+# CTAs whose partial results are merged with weights 2^(m_split - M).  The
+# cases below make both paths run: heads whose logits spread over tens of log2
+# units (q scaled by 16), heads whose winning row sits in a late tile of a
+# late split or in an early split (the other splits' weights underflow), and
+# heads whose winning row is a window row.
+LOG2E = 1.4426950408889634
+
+
+def _attn_splits(nq, n_rows_max):
+    """The number of CTAs per query the library uses (the rule of its planner)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = (n_rows_max + 127) // 128
+    return max(1, min(sms // nq, tiles, 8))
+
+
+def _split_tiles(n_rows, splits):
+    """Row ranges of the 128-row tiles of each split (ceil division of the tiles)."""
+    tiles = (n_rows + 127) // 128
+    tps = (tiles + splits - 1) // splits
+    out = []
+    for s in range(splits):
+        t0, t1 = min(tiles, s * tps), min(tiles, s * tps + tps)
+        out.append([(128 * t, min(n_rows, 128 * t + 128)) for t in range(t0, t1)])
+    return out
+
+
+def _sel_rows(wl, b, sel, win_bits, wcap, t, n_win):
+    """The oracle's row set of one query: its selected entries (encoded from the
+    generator's latents of just those entries), then its window rows."""
+    C, _ = ci.latent_rows_at(wl, b, sel, "cpu")
+    key = np.zeros((1, len(sel), wl.d_idx), np.float32)
+    codes, scales, _k, _s, _x, _ = O.append(C.reshape(1, -1, 512).numpy(), None, key, 1)
+    return O.gather_rows(codes, scales, 0, np.arange(len(sel), dtype=np.int32), win_bits, wcap, t,
+                         0, n_win)
+
+
+def _peaky_q(rng, rows, cnt, H):
+    """Attention queries (fp32) of one query whose rows are `rows` (selected
+    entries first, then the window): heads 0-15 random at 16x the usual scale;
+    16-31 aligned with a row three quarters into the selection; 32-47 aligned
+    with a row an eighth into it; 48-55 aligned with one of the last window
+    rows; 56-63 the usual N(0, 1/512)."""
+    q = rng.normal(size=(H, 512)) / np.sqrt(512.0)
+    q[:16] *= 16.0
+    for h in range(16, 32):
+        q[h] = rows[int(cnt * 0.75) + (h - 16) * (cnt // 80)] * (0.05 + 0.01 * (h - 16))
+    for h in range(32, 48):
+        q[h] = rows[cnt // 8 + (h - 32) * 3] * 0.08
+    n_w = len(rows) - cnt
+    for h in range(48, 56):
+        q[h] = rows[cnt + n_w - 4 + (h % 4)] * 0.1
+    return q
+
+
+def _f32_of_bits(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("layout", ["one_split", "eight_splits"])
+def test_attention_peaky_logits_rescale_and_split_merge(layout):
+    H, n_win, wcap = 64, 128, 256
+    if layout == "one_split":
+        # 160 queries, one CTA each; three of them hold 2,048 selected rows (17
+        # tiles in one CTA), the others a handful
+        n_ent, nq = 2200, 160
+        cnts = [16 + (i % 5) for i in range(nq)]
+        big = [0, 77, 159]
+        for i in big:
+            cnts[i] = 2048
+    else:
+        # two queries split 8 ways: 8,000 + 128 rows (8 tiles per CTA) and 2,048 + 128
+        n_ent, nq = 12000, 2
+        cnts = [8000, 2048]
+        big = [0, 1]
+    wl = ci.Workload("t", nq, [n_ent] * nq, 0, 1, heads=H, seed=36)
+    cache = build_gpu_cache(wl, DEV)
+    rng = np.random.default_rng(36)
+    k_max = max(cnts)
+    idx = np.zeros((nq, k_max), np.int32)
+    for i, c in enumerate(cnts):
+        idx[i, :c] = np.sort(rng.choice(n_ent, c, replace=False))
+    win = ci.window_rows(wl, nq, wcap, "cpu")
+    t = n_ent - 1
+    rows_of, q = {}, np.zeros((nq, H, 512))
+    for i in range(nq):
+        rows_of[i] = _sel_rows(wl, i, idx[i, :cnts[i]], bits16(win[i]), wcap, t, n_win)
+        if i in big:
+            q[i] = _peaky_q(rng, rows_of[i], cnts[i], H)
+        else:
+            q[i] = rng.normal(size=(H, 512)) / np.sqrt(512.0)
+    qa = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+    splits = _attn_splits(nq, k_max + n_win)
+    assert splits == (1 if layout == "one_split" else 8)
+    # the inputs drive the paths under test (checked on exact logits)
+    rescaled_late, far_apart = False, False
+    for i in big:
+        lg = (rows_of[i] @ _f32_of_bits(bits16(qa[i])).T) * LOG2E       # [rows][H], log2 units
+        parts = [p for p in _split_tiles(len(rows_of[i]), splits) if p]
+        for tiles in parts:
+            if len(tiles) > 1:
+                first = lg[tiles[0][0]:tiles[0][1]].max(0)
+                later = np.max([lg[a:b].max(0) for a, b in tiles[1:]], axis=0)
+                rescaled_late |= bool((later > first + 8).any())
+        if len(parts) > 1:
+            sm = np.sort(np.array([lg[p[0][0]:p[-1][1]].max(0) for p in parts]), axis=0)
+            far_apart |= bool(((sm[-1] - sm[-2]) > 20).any())
+    assert rescaled_late
+    assert far_apart or layout == "one_split"
+    out = torch.full((nq, H, 512), float("nan"), device=DEV)
+    lse = torch.full((nq, H), float("nan"), device=DEV)
+    cnt = csa.new_counters()
+    qs = csa.Queries(list(range(nq)), [t] * nq, 1, DEV)
+    csa.sparse_attn(cache, qs, torch.from_numpy(idx).to(DEV),
+                    torch.tensor(cnts, dtype=torch.int32, device=DEV), qa.to(DEV), win.to(DEV),
+                    n_win, out, lse=lse, counters=cnt)
+    torch.cuda.synchronize()
+    assert _np(cnt).tolist() == [0, 0, 0, 0]
+    go, gl = _np(out), _np(lse)
+    for i in range(nq):
+        ref, rlse = O.attention(bits16(qa[i]), rows_of[i], 1.0)
+        err = rel_rows(go[i], ref)
+        assert err.max() <= TOL, (i, int(err.argmax()), float(err.max()))
+        assert np.abs(gl[i] - rlse).max() <= 1e-3 * max(1.0, np.abs(rlse).max()), i

@@ -2,13 +2,16 @@
 (for instance a plugin whose host program owns every device allocation, or a
 serving loop that forbids allocating after start-up).  Its scratch is a fixed
 array inside the library.  The test calls it through the C ABI and compares
-it with csa2_topk, the entry point that takes a workspace, on two calls in a
-row: the second call must not see anything the first one left behind."""
+it with csa2_topk, the entry point that takes a workspace, and with the
+float64 oracle's top-k, on two calls in a row: the second call must not see
+anything the first one left behind."""
 import ctypes
 
 import pytest
+import numpy as np
 import torch
 
+import oracle as O
 import sparse_attention_decode_step_gb300 as csa
 from helpers import need_gpu
 
@@ -59,6 +62,12 @@ def test_noalloc_topk_matches_workspace_topk_twice():
         assert torch.equal(cnt_a, cnt_b)
         assert torch.equal(idx_a, idx_b)
         assert int(cnt_a.min()) == min(k, n - 3 * (nq - 1))
+        # and both equal the oracle's selection on the same fp32 scores
+        s_h, nv_h = scores.cpu().numpy(), nv.cpu().numpy()
+        ia, ca = idx_a.cpu().numpy(), cnt_a.cpu().numpy()
+        for i in range(nq):
+            ref = O.topk(s_h[i, :nv_h[i]], k)
+            assert ca[i] == len(ref) and np.array_equal(ia[i, :ca[i]], ref), (seed, i)
 
 
 def test_noalloc_topk_refuses_problems_beyond_its_scratch():
