@@ -110,10 +110,11 @@ class _Nvml:
 
 
 class Clocks:
-    """SM clock, power and clock-event reasons sampled every 10 ms during the
-    timed region, in-process through NVML (read-only queries) on a background
-    thread; if NVML cannot be used, an nvidia-smi child process queries the
-    same device by UUID.  Errors are kept in the summary."""
+    """SM clock, power and clock-event reasons sampled every millisecond during
+    the timed region, in-process through NVML (read-only queries) on a
+    background thread; if NVML cannot be used, an nvidia-smi child process
+    queries the same device by UUID every 10 ms.  Errors are kept in the
+    summary."""
 
     def __init__(self, index):
         self.index = index
@@ -137,7 +138,7 @@ class Clocks:
                     except Exception as e:   # keep sampling; record the first error
                         if len(self.errors) < 3:
                             self.errors.append(f"nvml sample: {e}")
-                    self._stop.wait(0.01)
+                    self._stop.wait(0.001)
             self._thr = threading.Thread(target=loop, daemon=True)
             self._thr.start()
             self.proc = None
@@ -297,6 +298,13 @@ def run_csa2(args, rank, world):
         csa.sparse_attn(cache, qs, idx, cnt, stage["q"], win, wl.n_win, out, lse=lse,
                         ws=aws, counters=counters)
 
+    # the step as a serving loop runs it: the append, then the layer call
+    # (csa2_layer_step: indexer with the top-k's first histogram, top-k, attention)
+    layer = csa.Layer(csa.FULL, cache, qs, k=wl.k, q=stage["q"], win=win, n_win=wl.n_win, out=out,
+                      idx=idx, cnt=cnt, q_idx=stage["q_idx"], w=stage["w"], max_n=max_n, lse=lse,
+                      counters=counters)
+    step_fns = [ph_append, layer]
+    # the same work as separate library calls, one graph each, for the phase split
     phase_fns = [ph_append, ph_index, ph_topk, ph_attn]
     appended = [0]
 
@@ -313,7 +321,7 @@ def run_csa2(args, rank, world):
     l0 = csa.launch_count()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=side):
-        for f in phase_fns:
+        for f in step_fns:
             f()
     launches_per_step = csa.launch_count() - l0
     pgraphs = []
@@ -385,6 +393,7 @@ def run_csa2(args, rank, world):
 
     t_index = timed_call(ph_index)
     t_attn = timed_call(ph_attn)
+    t_layer = timed_call(layer)
     # the append variant whose indexer keys are projected from the stored
     # entries (random-init bf16 W_IK), the same 32 new tokens
     g = torch.Generator(device=dev).manual_seed(7)
@@ -415,9 +424,13 @@ def run_csa2(args, rank, world):
         "config": {"workload": wl.name, "batch": B, "ctx_tokens": T0 + 1, "m": wl.m,
                    "indexer_heads": wl.h_idx, "d_idx": wl.d_idx, "heads": wl.heads, "k": wl.k,
                    "n_win": wl.n_win, "layers": 1, "l2": "flushed between steps (512 MB write)",
-                   "graph": "one CUDA graph replay per step", "parallelism": f"replicas x{world}"},
+                   "graph": "one CUDA graph replay per step (csa2_quantize_append + "
+                            "csa2_layer_step)", "parallelism": f"replicas x{world}"},
         "phases_us": {"append": round(ph[0] * 1e6, 2), "index_full": round(ph[1] * 1e6, 2),
-                      "topk": round(ph[2] * 1e6, 2), "sparse_attn": round(ph[3] * 1e6, 2)},
+                      "topk": round(ph[2] * 1e6, 2), "sparse_attn": round(ph[3] * 1e6, 2),
+                      "note": "the step's work as separate library calls, one graph each; the "
+                              "timed step is the append plus one csa2_layer_step call"},
+        "layer_call_us": round(t_layer * 1e6, 2),
         "attn_roofline": {"kernel": "attn_tc_kernel (one csa2_sparse_attn call)", "bound": "hbm",
                           "achieved": round(attn_bytes / t_attn / 1e9, 1), "peak": hbm,
                           "unit": "GB/s", "frac": round(attn_bytes / t_attn / 1e9 / hbm, 4),

@@ -80,12 +80,14 @@ int attn_plan(int nq, int k_max, int n_win)
     return s;
 }
 
-// The splits of a query merge on chip (distributed shared memory): the
-// attention needs no workspace.
+// A query split over several CTAs merges through a workspace slot per split
+// (its scaled partial output, [64 heads][512] fp32); a query that is one CTA
+// writes its output directly.
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win)
 {
-    (void)nq; (void)H; (void)k_max; (void)n_win;
-    return 0;
+    (void)H;
+    const int s = attn_plan(nq, k_max, n_win);
+    return s > 1 ? (size_t)nq * s * 64 * CSA2_D * sizeof(float) : 0;
 }
 
 }  // namespace csa2
@@ -199,11 +201,17 @@ csa2_status csa2_quantize_append_project(const csa2_cache *cache, const float *C
                                              static_cast<cudaStream_t>(stream)));
 }
 
-csa2_status csa2_index_full(const csa2_cache *cache, const csa2_queries *queries,
+}  // extern "C"
+
+namespace {
+
+// The entry points' bodies; hist0 (nullable, [nq][2048]) is filled by the
+// decode indexer for the top-k that follows inside csa2_layer_step.
+csa2_status index_full_impl(const csa2_cache *cache, const csa2_queries *queries,
                             const float *q_idx, const float *w, int32_t h_idx, int64_t max_n,
                             float *scores, int64_t ld_scores, float *blockmax,
                             int64_t ld_blockmax, int32_t *n_valid, void *workspace,
-                            size_t ws_bytes, uint32_t *counters, void *stream)
+                            size_t ws_bytes, uint32_t *counters, uint32_t *hist0, void *stream)
 {
     csa2_status s = check_index_args(cache, queries, q_idx, w, h_idx, scores, ld_scores, workspace);
     if (s != CSA2_OK) return s;
@@ -219,15 +227,15 @@ csa2_status csa2_index_full(const csa2_cache *cache, const csa2_queries *queries
                  CSA2_ERR_CAPACITY);
     return cuda_status(launch_index(*cache, *queries, q_idx, w, h_idx, max_n, nullptr, nullptr, 0,
                                     scores, ld_scores, blockmax, ld_blockmax, n_valid, workspace,
-                                    counters, static_cast<cudaStream_t>(stream)));
+                                    counters, hist0, static_cast<cudaStream_t>(stream)));
 }
 
-csa2_status csa2_index_reindex(const csa2_cache *cache, const csa2_queries *queries,
+csa2_status index_reindex_impl(const csa2_cache *cache, const csa2_queries *queries,
                                const float *q_idx, const float *w, int32_t h_idx,
                                const int32_t *pool_blk, const int32_t *pool_n,
                                int32_t pool_blocks, float *scores, int64_t ld_scores,
                                int32_t *n_valid, void *workspace, size_t ws_bytes,
-                               uint32_t *counters, void *stream)
+                               uint32_t *counters, uint32_t *hist0, void *stream)
 {
     csa2_status s = check_index_args(cache, queries, q_idx, w, h_idx, scores, ld_scores, workspace);
     if (s != CSA2_OK) return s;
@@ -241,13 +249,13 @@ csa2_status csa2_index_reindex(const csa2_cache *cache, const csa2_queries *quer
                  CSA2_ERR_CAPACITY);
     return cuda_status(launch_index(*cache, *queries, q_idx, w, h_idx, 8LL * pool_blocks, pool_blk,
                                     pool_n, pool_blocks, scores, ld_scores, nullptr, 0, n_valid,
-                                    workspace, counters, static_cast<cudaStream_t>(stream)));
+                                    workspace, counters, hist0, static_cast<cudaStream_t>(stream)));
 }
 
-csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_valid,
+csa2_status topk_impl(const float *scores, int64_t ld_scores, const int32_t *n_valid,
                       const int32_t *pool_blk, int32_t pool_blocks, int32_t nq, int64_t max_n,
                       int32_t k, int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out,
-                      void *workspace, size_t ws_bytes, void *stream)
+                      void *workspace, size_t ws_bytes, const uint32_t *hist0, void *stream)
 {
     CSA2_REQUIRE(nq >= 0, CSA2_ERR_INVALID_ARG);
     if (nq == 0) return CSA2_OK;
@@ -264,8 +272,43 @@ csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_v
     CSA2_REQUIRE(max_n < (1LL << 31), CSA2_ERR_INVALID_ARG);
     CSA2_REQUIRE(ws_bytes >= topk_workspace_bytes(nq, max_n), CSA2_ERR_CAPACITY);
     return cuda_status(launch_topk(scores, ld_scores, n_valid, 0, pool_blk, pool_blocks, nq, max_n,
-                                   k, idx_out, ld_idx, cnt_out, workspace,
+                                   k, idx_out, ld_idx, cnt_out, workspace, hist0,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+csa2_status csa2_index_full(const csa2_cache *cache, const csa2_queries *queries,
+                            const float *q_idx, const float *w, int32_t h_idx, int64_t max_n,
+                            float *scores, int64_t ld_scores, float *blockmax,
+                            int64_t ld_blockmax, int32_t *n_valid, void *workspace,
+                            size_t ws_bytes, uint32_t *counters, void *stream)
+{
+    return index_full_impl(cache, queries, q_idx, w, h_idx, max_n, scores, ld_scores, blockmax,
+                           ld_blockmax, n_valid, workspace, ws_bytes, counters, nullptr, stream);
+}
+
+csa2_status csa2_index_reindex(const csa2_cache *cache, const csa2_queries *queries,
+                               const float *q_idx, const float *w, int32_t h_idx,
+                               const int32_t *pool_blk, const int32_t *pool_n,
+                               int32_t pool_blocks, float *scores, int64_t ld_scores,
+                               int32_t *n_valid, void *workspace, size_t ws_bytes,
+                               uint32_t *counters, void *stream)
+{
+    return index_reindex_impl(cache, queries, q_idx, w, h_idx, pool_blk, pool_n, pool_blocks,
+                              scores, ld_scores, n_valid, workspace, ws_bytes, counters, nullptr,
+                              stream);
+}
+
+csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_valid,
+                      const int32_t *pool_blk, int32_t pool_blocks, int32_t nq, int64_t max_n,
+                      int32_t k, int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out,
+                      void *workspace, size_t ws_bytes, void *stream)
+{
+    return topk_impl(scores, ld_scores, n_valid, pool_blk, pool_blocks, nq, max_n, k, idx_out,
+                     ld_idx, cnt_out, workspace, ws_bytes, nullptr, stream);
 }
 
 csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const int32_t *n_valid,
@@ -286,12 +329,19 @@ csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const i
                                    static_cast<cudaStream_t>(stream)));
 }
 
-csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *queries,
+}  // extern "C"
+
+namespace {
+
+// early: the kernel launched just before on the stream (this library's top-k
+// inside csa2_layer_step) writes none of q, win or the cache, so the attention
+// may load q before its programmatic dependent-launch wait.
+csa2_status sparse_attn_impl(const csa2_cache *cache, const csa2_queries *queries,
                              const int32_t *idx, int64_t ld_idx, const int32_t *cnt,
                              int32_t k_max, const uint16_t *q, int32_t H, const uint16_t *win,
                              int32_t wcap, const int32_t *win_start, int32_t n_win,
                              float sm_scale, float *out, float *lse, void *workspace,
-                             size_t ws_bytes, uint32_t *counters, void *stream)
+                             size_t ws_bytes, uint32_t *counters, int early, void *stream)
 {
     csa2_status s = check_cache(cache, false);
     if (s != CSA2_OK) return s;
@@ -307,7 +357,10 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
                      (cnt == nullptr || al4(cnt)) && (win == nullptr || al16(win)) &&
                      (win_start == nullptr || al4(win_start)) && (lse == nullptr || al4(lse)),
                  CSA2_ERR_ALIGN);
-    CSA2_REQUIRE(ws_bytes >= attn_workspace_bytes(queries->nq, H, k_max, n_win), CSA2_ERR_CAPACITY);
+    const size_t need = attn_workspace_bytes(queries->nq, H, k_max, n_win);
+    CSA2_REQUIRE(ws_bytes >= need, CSA2_ERR_CAPACITY);
+    CSA2_REQUIRE(need == 0 || (workspace != nullptr && al16(workspace)),
+                 workspace == nullptr ? CSA2_ERR_INVALID_ARG : CSA2_ERR_ALIGN);
     AttnParams p{};
     p.codes = cache->codes;
     p.scales = cache->scales;
@@ -332,9 +385,25 @@ csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *querie
     p.out = out;
     p.lse = lse;
     p.splits = attn_plan(p.nq, k_max, n_win);
-    (void)workspace;
+    p.part = need > 0 ? static_cast<float *>(workspace) : nullptr;
     p.counters = counters;
+    p.early = early;
     return cuda_status(launch_attn_tc(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *queries,
+                             const int32_t *idx, int64_t ld_idx, const int32_t *cnt,
+                             int32_t k_max, const uint16_t *q, int32_t H, const uint16_t *win,
+                             int32_t wcap, const int32_t *win_start, int32_t n_win,
+                             float sm_scale, float *out, float *lse, void *workspace,
+                             size_t ws_bytes, uint32_t *counters, void *stream)
+{
+    return sparse_attn_impl(cache, queries, idx, ld_idx, cnt, k_max, q, H, win, wcap, win_start,
+                            n_win, sm_scale, out, lse, workspace, ws_bytes, counters, 0, stream);
 }
 
 // ---------------------------------------------------------------- layer driver
@@ -343,7 +412,8 @@ namespace {
 struct LayerPlan {
     int64_t max_n, ld, ld_bm;
     int chunk;                    // queries per indexer/top-k chunk
-    size_t off_scores, off_bm, off_nv, off_idx_ws, off_topk_ws, off_attn_ws, total;
+    bool hist;                    // the indexer counts the top-k's first histogram
+    size_t off_scores, off_bm, off_nv, off_hist, off_idx_ws, off_topk_ws, off_attn_ws, total;
 };
 
 bool plan_layer(const csa2_layer_args *a, LayerPlan *pl)
@@ -370,6 +440,9 @@ bool plan_layer(const csa2_layer_args *a, LayerPlan *pl)
         if (a->mode == CSA2_FULL && a->build_pool) o += align_up((size_t)chunk * pl->ld_bm * 4, 256);
         pl->off_nv = o;
         o += align_up((size_t)nq * 4, 256);
+        pl->hist = (a->mode == CSA2_REINDEX || group == 1) && topk_select_fits(pl->max_n, a->k);
+        pl->off_hist = o;
+        if (pl->hist) o += align_up((size_t)chunk * 2048 * 4, 256);
         pl->off_idx_ws = o;
         o += align_up(index_workspace_bytes((int)chunk, a->mode == CSA2_FULL ? group : 1, a->h_idx,
                                             a->cache->d_idx),
@@ -424,6 +497,7 @@ csa2_status csa2_layer_step(const csa2_layer_args *a, void *stream)
         float *scores = reinterpret_cast<float *>(ws + pl.off_scores);
         float *bm = reinterpret_cast<float *>(ws + pl.off_bm);
         int32_t *nv = reinterpret_cast<int32_t *>(ws + pl.off_nv);
+        uint32_t *hist = pl.hist ? reinterpret_cast<uint32_t *>(ws + pl.off_hist) : nullptr;
         void *iws = ws + pl.off_idx_ws;
         void *tws = ws + pl.off_topk_ws;
         const size_t iws_bytes = pl.off_topk_ws - pl.off_idx_ws;
@@ -439,18 +513,18 @@ csa2_status csa2_layer_step(const csa2_layer_args *a, void *stream)
             int32_t *pblk = a->pool_blk ? a->pool_blk + (int64_t)q0 * a->pool_blocks : nullptr;
             int32_t *pn = a->pool_n ? a->pool_n + q0 : nullptr;
             if (a->mode == CSA2_FULL) {
-                s = csa2_index_full(a->cache, &sub, qi, wi, a->h_idx, pl.max_n, scores, pl.ld,
+                s = index_full_impl(a->cache, &sub, qi, wi, a->h_idx, pl.max_n, scores, pl.ld,
                                     a->build_pool ? bm : nullptr, pl.ld_bm, nv + q0, iws,
-                                    iws_bytes, a->counters, stream);
+                                    iws_bytes, a->counters, hist, stream);
             } else {
-                s = csa2_index_reindex(a->cache, &sub, qi, wi, a->h_idx, pblk, pn, a->pool_blocks,
-                                       scores, pl.ld, nv + q0, iws, iws_bytes, a->counters,
+                s = index_reindex_impl(a->cache, &sub, qi, wi, a->h_idx, pblk, pn, a->pool_blocks,
+                                       scores, pl.ld, nv + q0, iws, iws_bytes, a->counters, hist,
                                        stream);
             }
             if (s != CSA2_OK) return s;
-            s = csa2_topk(scores, pl.ld, nv + q0, a->mode == CSA2_REINDEX ? pblk : nullptr,
+            s = topk_impl(scores, pl.ld, nv + q0, a->mode == CSA2_REINDEX ? pblk : nullptr,
                           a->pool_blocks, nc, pl.max_n, a->k, a->idx + (int64_t)q0 * a->k, a->k,
-                          a->cnt + q0, tws, tws_bytes, stream);
+                          a->cnt + q0, tws, tws_bytes, hist, stream);
             if (s != CSA2_OK) return s;
             if (a->mode == CSA2_FULL && a->build_pool) {
                 s = csa2_pool_select(bm, pl.ld_bm, nv + q0, nc, pl.max_n, a->pool_blocks, pblk, pn,
@@ -459,9 +533,11 @@ csa2_status csa2_layer_step(const csa2_layer_args *a, void *stream)
             }
         }
     }
-    return csa2_sparse_attn(a->cache, a->queries, a->idx, a->k, a->cnt, a->k, a->q, a->H, a->win,
+    // after this call's own top-k, the attention may load its queries early
+    return sparse_attn_impl(a->cache, a->queries, a->idx, a->k, a->cnt, a->k, a->q, a->H, a->win,
                             a->wcap, a->win_start, a->n_win, a->sm_scale, a->out, a->lse,
-                            ws + pl.off_attn_ws, pl.total - pl.off_attn_ws, a->counters, stream);
+                            ws + pl.off_attn_ws, pl.total - pl.off_attn_ws, a->counters,
+                            a->mode != CSA2_REUSE ? 1 : 0, stream);
 }
 
 const char *csa2_status_string(csa2_status s)

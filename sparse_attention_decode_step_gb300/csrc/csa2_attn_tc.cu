@@ -21,19 +21,26 @@
 // more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
 // in TMEM.
 //
-// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  V is gathered and
-// dequantised in four 128-channel chunks (8 rows x 64 code bytes per warp
-// load, 16 code bytes and 2 scale bytes per lane), each chunk with its own
-// barrier, so the QK product of chunk c runs while chunk c + 1 is stored; the
-// next tile's codes are loaded in two halves, during the tail of the QK
-// product and during the PV product.  In the softmax a worker owns half of a
-// tile row (32 heads), two per TMEM lane quarter.  The cross-row max reduction runs only when a logit exceeds its
-// head's reference max by more than 8 (always on the first tile); row sums are
-// reduced once per tile.  The splits of a query (at most 8) form a thread-block
-// cluster: every CTA sends its reference max and sum to all peers, scales its
-// O^T by 2^(m_s - M) / L and stores each 32-channel chunk into the shared
-// memory of the CTA that owns the chunk, which sums the splits' chunks and
-// writes the output.  Nothing goes through global memory between splits.
+// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  V is gathered with 8
+// lanes per row (128 contiguous code bytes = one 128-byte line per row, 4 rows
+// per warp load) and dequantised in two 256-channel chunks, each with its own
+// barrier.  The chunks are pipelined across tiles: the PV product of tile i
+// releases chunk 0 of the V tile after its first two channel blocks, so the
+// workers store chunk 0 of tile i + 1 while PV finishes, and the QK product of
+// tile i + 1 over chunk 0 runs while chunk 1 is stored.  The next tile's codes
+// are loaded as soon as this tile's chunks are stored (during the QK product
+// and the softmax); the rows of the tile after that are asked of L2 one tile
+// earlier.  In the softmax a worker owns half of a tile row (32 heads), two per
+// TMEM lane quarter.  The cross-row max reduction runs only when a logit
+// exceeds its head's reference max by more than 8 (always on the first tile);
+// each thread keeps its rows' sums and they are reduced once, at the end.  The
+// splits of a query (at most 8) form a thread-block cluster: every CTA sends
+// its reference max and sum to all peers through distributed shared memory,
+// writes its O^T scaled by 2^(m_s - M) / L to its slot of a workspace (L2),
+// and after a cluster barrier the CTA that owns a 32-channel chunk sums the
+// splits' slots for it and writes the output.  The set-up that reads nothing
+// the previous kernel writes (barriers, TMEM, and inside a layer step the
+// query block) runs before the programmatic-dependent-launch wait.
 #include <cooperative_groups.h>
 
 #include "csa2_device.cuh"
@@ -250,10 +257,6 @@ __device__ __forceinline__ void named_sync_all_workers()
     asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-// Cluster merge: a block of the receive area is one 32-channel chunk of one
-// split, [64 heads][32 channels] fp32 (8 KB), so that a warp (lane = channel)
-// writes and reads 128 contiguous bytes per head.
-constexpr int kXBlock = 64 * 32;
 constexpr int kMaxClusterSplits = 8;
 
 __device__ __forceinline__ void cluster_arrive()
@@ -268,8 +271,6 @@ __device__ __forceinline__ void cluster_wait()
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 {
-    pdl_wait();
-    pdl_trigger();
     const int q = blockIdx.y, split = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -287,14 +288,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     float *sRedL = sL + 64;                   // [4 quarters][64 heads] tile row sums
     float *sML = sRedL + 4 * 64;              // cluster merge: [split][m | l][64 heads]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sML + kMaxClusterSplits * 2 * 64);
-    uint64_t *bar_v = bars;                   // [4]: V channel chunk c stored
-    uint64_t *bar_s = bars + 4, *bar_p = bars + 5, *bar_o = bars + 6;
-    uint64_t *bar_done = bars + 7, *bar_q = bars + 8;
+    uint64_t *bar_v = bars;                   // [2]: V channel chunk h (256 channels) stored
+    uint64_t *bar_s = bars + 2, *bar_p = bars + 3;
+    uint64_t *bar_o = bars + 4;               // [2]: PV channel blocks 2h, 2h + 1 done
+    uint64_t *bar_done = bars + 6, *bar_q = bars + 7;
     int *sFlag = reinterpret_cast<int *>(bars + 9);   // [0] abort [1] rescale [2] bad [3] need max
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sFlag + 4);
     volatile int *abort_flag = sFlag;
 
+    // ---- set-up that reads nothing an earlier kernel writes: barriers, TMEM, and
+    // (p.early) the query block, whose bulk copy lands in the still-free V tile
+    if (tid == 0) {
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(&bar_v[c], kWorkers / 32);
+            mbar_init(&bar_o[c], 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, kWorkers / 32);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_q, 1);
+        sFlag[0] = 0;
+        sFlag[1] = 0;
+        sFlag[2] = 0;
+        sFlag[3] = 0;
+        fence_barrier_init();
+    }
+    if (tid < 64) { sM[tid] = -INFINITY; sAlpha[tid] = 1.f; sL[tid] = 0.f; }
+    // a CTA's shared memory may be written by its cluster peers only once it runs:
+    // arrive now, wait before the first remote store (the merge at the end)
+    cluster_arrive();
+    __syncthreads();
+    auto load_q = [&]() {
+        const uint32_t qbytes = (uint32_t)H * CSA2_D * 2;
+        mbar_arrive_expect_tx(bar_q, qbytes);
+        bulk_load(sV, p.q + (int64_t)q * H * CSA2_D, qbytes, bar_q);
+    };
+    if (tid == 0 && p.early) load_q();
+    if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
+    pdl_wait();
+    pdl_trigger();
+    if (tid == 0 && !p.early) load_q();
+
     const TcRowSet rs = tc_row_set(p, q);
+    if (tid == 0 && rs.bad) sFlag[2] = 1;
     const int n_rows = rs.cnt + rs.nw;
     // this query's tiles, ceil(tiles / splits) per split: the last split, which
     // holds the window rows (the slower tile), gets the remainder
@@ -306,48 +342,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int r_end = min(n_rows, t_end * kRows);
     const int n_tiles = t_end - t_begin;
 
-    if (tid == 0) {
-        for (int c = 0; c < 4; ++c) mbar_init(&bar_v[c], kWorkers / 32);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_p, kWorkers / 32);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_done, 1);
-        mbar_init(bar_q, 1);
-        sFlag[0] = 0;
-        sFlag[1] = 0;
-        sFlag[2] = rs.bad ? 1 : 0;
-        sFlag[3] = 0;
-        fence_barrier_init();
-    }
-    if (tid < 64) { sM[tid] = -INFINITY; sAlpha[tid] = 1.f; sL[tid] = 0.f; }
-    // a CTA's shared memory may be written by its cluster peers only once it runs:
-    // arrive now, wait before the first remote store (the merge at the end)
-    cluster_arrive();
-    if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
-
-    // ---- Q: one bulk copy of the raw bf16 block [H][512] into the (still free)
-    // V tile, then bf16 -> f16 into the K-major 128-byte-swizzled sQ; heads >= H are zero
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t qbytes = (uint32_t)H * CSA2_D * 2;
-        mbar_arrive_expect_tx(bar_q, qbytes);
-        bulk_load(sV, p.q + (int64_t)q * H * CSA2_D, qbytes, bar_q);
-    }
-    // the worker threads start gathering the first tile's rows meanwhile (below)
+    // ---- Q: the raw bf16 block [H][512] lands in the V tile, then bf16 -> f16 into
+    // the K-major 128-byte-swizzled sQ (heads >= H are zero); the worker threads
+    // start gathering the first tile's rows meanwhile (below)
     const int wt = tid - 32;                          // worker index 0..255
     const uint32_t quarter = (uint32_t)(warp & 3);    // TMEM lanes 32 quarter ..
     const int row = (int)(quarter * 32 + lane);       // tile row == TMEM lane of this thread
     const int half = (warp - 1) >> 2;                 // heads 32 half .. of its softmax
 
-    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15, one 128-channel
-    // chunk c (atom columns 2c, 2c + 1) at a time, so that the QK product of chunk c
-    // runs while the later chunks are dequantised.  In load x (0, 1) of chunk c, lane l
-    // takes row 8x + (l >> 2) of the warp's 16 and channels 128c + 32 (l & 3) .. + 31
-    // (16 code bytes, 2 scale bytes) into register slot t = 2c + x; as soon as chunk c
-    // of this tile is stored, the slot is refilled with chunk c of the next tile.
+    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15.  A warp load
+    // covers 4 rows with 8 lanes each: lane l takes row 4x + (l >> 3) of the warp's
+    // 16 and, in channel chunk h (channels 256h ..), the 32 channels 256h + 32 sub ..
+    // (sub = l & 7): 16 contiguous code bytes and 2 scale bytes, so that each row's
+    // 8 lanes read one 128-byte line.  Register slot t = 4h + x.
     const int wg = warp - 1;
-    const int sub = lane & 15;
-    const int s4 = lane & 3;
+    const int sub = lane & 7;
+    const int rho = sub >> 1;                          // store rotation (bank groups)
     uint4 gc[8];                  // codes of slot t
     uint32_t gsc[8];              // the two scale bytes of those channels
     uint32_t gkind = 0;           // bit t: FP4 row with data; bit 8 + t: window row
@@ -358,19 +368,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         const int g = tile_row(tile, r);
         return (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
     };
-    auto load_chunk = [&](int tile, int c) {
+    auto load_tile = [&](int tile) {
+        gkind = 0;
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            const int t = 2 * c + x;
-            const int rw = 8 * x + (lane >> 2);
+        for (int t = 0; t < 8; ++t) {
+            const int h = t >> 2, x = t & 3;
+            const int rw = 4 * x + (lane >> 3);
             const int g = tile_row(tile, 16 * wg + rw);
             const int j = __shfl_sync(0xffffffffu, gj, rw);
-            gkind &= ~((1u << t) | (1u << (8 + t)));
             if (g < r_end && g < rs.cnt) {
                 if (j >= 0 && j < rs.nt) {
                     const int64_t r = rs.base + j;
-                    gc[t] = __ldg(reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES) + 4 * c + s4);
-                    gsc[t] = __ldg(reinterpret_cast<const uint16_t *>(p.scales + r * CSA2_SCALE_BYTES) + 4 * c + s4);
+                    gc[t] = __ldg(reinterpret_cast<const uint4 *>(p.codes + r * CSA2_CODE_BYTES) + 8 * h + sub);
+                    gsc[t] = __ldg(reinterpret_cast<const uint16_t *>(p.scales + r * CSA2_SCALE_BYTES) + 8 * h + sub);
                     gkind |= 1u << t;
                 } else {
                     sFlag[2] = 1;
@@ -380,55 +390,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             }
         }
     };
-    // Chunk c of this warp's rows into sV.  A lane's 32 channels are the 16-byte
-    // pieces 4 (s4 & 1) .. + 3 of atom column 2c + (s4 >> 1).  16-byte stores are
-    // served 8 lanes (2 rows x 4 slices) at a time; the lanes of the second atom
-    // column (hi) take their pieces in an order rotated by 2 (v[k] = piece
-    // (k + 2) & 3, so the code words and scale bytes are swapped on input), which
-    // puts the 8 lanes of each group on 8 different 16-byte bank groups.
-    const int hi = s4 >> 1;
-    auto store_chunk = [&](int tile, int c) {
+    // Chunk h of this warp's rows into sV.  A lane's 32 channels are the 16-byte
+    // pieces 4 (sub & 1) .. + 3 of atom column 4h + (sub >> 1).  A 16-byte store is
+    // served 8 lanes (one row) at a time; lane sub writes, in its m-th store, piece
+    // 4 (sub & 1) + ((m + rho) & 3), so that the 8 lanes of a row hit 8 different
+    // 16-byte bank groups (the source words are rotated to match).
+    auto store_chunk = [&](int tile, int h) {
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            const int t = 2 * c + x;
-            const int r = 16 * wg + 8 * x + (lane >> 2);
+        for (int x = 0; x < 4; ++x) {
+            const int t = 4 * h + x;
+            const int r = 16 * wg + 4 * x + (lane >> 3);
             uint4 v[4];
             if (gkind & (1u << t)) {
-                const uint32_t sc = hi ? (gsc[t] >> 8) | (gsc[t] << 8) : gsc[t];
-                const uint32_t p0 = scale_pair(sc & 0xFFu), p1 = scale_pair((sc >> 8) & 0xFFu);
-                const uint4 g = gc[t];
-                v[0] = fp4x8_to_f16(hi ? g.z : g.x, p0);
-                v[1] = fp4x8_to_f16(hi ? g.w : g.y, p0);
-                v[2] = fp4x8_to_f16(hi ? g.x : g.z, p1);
-                v[3] = fp4x8_to_f16(hi ? g.y : g.w, p1);
+                const uint32_t p0 = scale_pair(gsc[t] & 0xFFu), p1 = scale_pair((gsc[t] >> 8) & 0xFFu);
+                uint32_t w[4] = {gc[t].x, gc[t].y, gc[t].z, gc[t].w};
+                uint32_t sp[4] = {p0, p0, p1, p1};
+                if (rho & 1) {
+                    const uint32_t w0 = w[0], s0 = sp[0];
+                    w[0] = w[1]; w[1] = w[2]; w[2] = w[3]; w[3] = w0;
+                    sp[0] = sp[1]; sp[1] = sp[2]; sp[2] = sp[3]; sp[3] = s0;
+                }
+                if (rho & 2) {
+                    uint32_t a = w[0], b = w[1];
+                    w[0] = w[2]; w[1] = w[3]; w[2] = a; w[3] = b;
+                    a = sp[0]; b = sp[1];
+                    sp[0] = sp[2]; sp[1] = sp[3]; sp[2] = a; sp[3] = b;
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) v[m] = fp4x8_to_f16(w[m], sp[m]);
             } else if (gkind & (1u << (8 + t))) {
                 const int64_t pos = rs.lo + (tile_row(tile, r) - rs.cnt);
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 16 * c + 4 * s4;
+                    p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 32 * h + 4 * sub;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 raw = __ldg(src + ((k + 2 * hi) & 3));
-                    v[k] = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
+                for (int m = 0; m < 4; ++m) {
+                    const uint4 raw = __ldg(src + ((m + rho) & 3));
+                    v[m] = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
                                       bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
+                for (int m = 0; m < 4; ++m) v[m] = make_uint4(0, 0, 0, 0);
             }
-            uint8_t *dst = sV + (2 * c + hi) * kVAtom;
+            uint8_t *dst = sV + (4 * h + (sub >> 1)) * kVAtom;
 #pragma unroll
             for (int m = 0; m < 4; ++m)
                 *reinterpret_cast<uint4 *>(
-                    dst + sw128((uint32_t)r, (uint32_t)(4 * (s4 & 1) + ((m + 2 * hi) & 3)))) = v[m];
+                    dst + sw128((uint32_t)r, (uint32_t)(4 * (sub & 1) + ((m + rho) & 3)))) = v[m];
+        }
+    };
+    // The rows of the tile after the next one are asked of L2 one tile before
+    // their loads (lanes 0-15: row 16 wg + lane, entry j; gj2 holds the entries
+    // of that tile)
+    int gj2 = -1;
+    auto prefetch_rows = [&](int tile, int j) {
+        const int g = tile_row(tile, 16 * wg + (lane & 15));
+        if (lane < 16 && g < r_end && g < rs.cnt && j >= 0 && j < rs.nt) {
+            const int64_t r = rs.base + j;
+            const uint8_t *c = p.codes + r * CSA2_CODE_BYTES;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(c));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.scales + r * CSA2_SCALE_BYTES));
         }
     };
     int my_j = -1;                // entry of this thread's softmax row in the current tile
     if (warp > 0 && n_tiles > 0) {
-        gj = lane < 16 ? entry(0, 16 * wg + sub) : -1;
+        gj = lane < 16 ? entry(0, 16 * wg + (lane & 15)) : -1;
         my_j = entry(0, row);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) load_chunk(0, c);
-        if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + sub) : -1;
+        load_tile(0);
+        if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + (lane & 15)) : -1;
+        if (n_tiles > 2) gj2 = lane < 16 ? entry(2, 16 * wg + (lane & 15)) : -1;
     }
     {
         volatile int no_abort = 0;
@@ -451,6 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const uint32_t tmem = *sTmem;
     const uint32_t tS = tmem;                  // S^T: columns 0..63
     const uint32_t tO = tmem + 64;             // O^T block mb: columns 64 + 64 mb
+    const uint32_t tLsum = tmem + 320;         // running sums: columns 320 .. 383
 
     if (warp == 0) {
         // ============================================== MMA issuer
@@ -460,13 +492,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             const uint32_t v0 = smem_u32(sV), q0 = smem_u32(sQ), p0 = smem_u32(sP);
             for (int i = 0; i < n_tiles; ++i) {
                 bool run = true;
-                for (int c = 0; c < 4 && run; ++c) {
-                    // the K range of chunk c (channels 128c ..) as soon as it is stored
-                    if (!mbar_wait<true>(&bar_v[c], i & 1, abort_flag)) { run = false; break; }
+                for (int h = 0; h < 2 && run; ++h) {
+                    // the K range of chunk h (channels 256h ..) as soon as it is stored
+                    if (!mbar_wait<true>(&bar_v[h], i & 1, abort_flag)) { run = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int k8 = 0; k8 < 8; ++k8) {
-                        const int ks = 8 * c + k8;
+                    for (int k16 = 0; k16 < 16; ++k16) {
+                        const int ks = 16 * h + k16;
                         const uint32_t a = v0 + (ks >> 2) * kVAtom + (ks & 3) * 32;
                         const uint32_t b = q0 + (ks >> 2) * kQAtom + (ks & 3) * 32;
                         mma_f16(tS, smem_desc(a, 16, 1024, kLayoutSW128),
@@ -477,6 +509,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 mma_commit(bar_s);
                 if (!mbar_wait<true>(bar_p, i & 1, abort_flag)) { *abort_flag = 1; break; }
                 tc_fence_after();
+                // channel blocks 0, 1 (chunk 0 of V) then 2, 3 (chunk 1); each pair's
+                // completion releases its chunk of the V tile
 #pragma unroll
                 for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
@@ -487,8 +521,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                                 smem_desc(b, kVAtom, 1024, kLayoutSW128), id_pv,
                                 (i > 0 || ks > 0) ? 1u : 0u);
                     }
+                    if (mb & 1) mma_commit(&bar_o[mb >> 1]);
                 }
-                mma_commit(bar_o);
             }
             if (*abort_flag) count_event(p.counters, CSA2_CNT_TIMEOUT);
             // every MMA of this thread has completed before TMEM is released
@@ -500,29 +534,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         // ============================================== 8 worker warps
         const float l2s = p.sm_scale * 1.4426950408889634f;
         const int h0 = 32 * half;                      // this thread's heads h0 .. h0+31
+        // this thread's share of the running sums, its rows' P for heads h0 .. h0+31,
+        // accumulates in TMEM columns 320 + h0 .. (its lane = its row): rescaled with
+        // the reference max, reduced over the rows once, at the end
+        const uint32_t tL = tLsum + (uint32_t)h0 + ((quarter * 32u) << 16);
+        {
+            float z[32];
+#pragma unroll
+            for (int h = 0; h < 32; ++h) z[h] = 0.f;
+            tmem_st32(tL, z);
+            tmem_wait_st();
+        }
         bool ok = true;
         for (int i = 0; i < n_tiles && ok; ++i) {
-            if (i > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_o, (i - 1) & 1, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-            }
+            if (i + 2 < n_tiles) prefetch_rows(i + 2, gj2);
             const int g_row = tile_row(i, row);
             const bool valid = g_row < r_end && (g_row >= rs.cnt || (my_j >= 0 && my_j < rs.nt));
+            // chunk h of this tile goes where the previous tile's PV product has
+            // released it (its channel blocks 2h, 2h + 1 done)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                store_chunk(i, c);
+            for (int h = 0; h < 2; ++h) {
+                if (i > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait<true>(&bar_o[h], (i - 1) & 1, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                store_chunk(i, h);
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_v[c]);
+                if (lane == 0) mbar_arrive(&bar_v[h]);
             }
-            // the next tile's codes: chunks 0 and 1 while the QK product finishes,
-            // chunks 2 and 3 while the PV product runs (issuing these loads takes
-            // about as long as either product)
+            if (!ok) break;
+            // the next tile's codes, in flight during the QK product and the softmax
             const bool more = i + 1 < n_tiles;
+            int my_j_next = -1;
             if (more) {
-                load_chunk(i + 1, 0);
-                load_chunk(i + 1, 1);
+                load_tile(i + 1);
+                gj = gj2;
+                if (i + 3 < n_tiles) gj2 = lane < 16 ? entry(i + 3, 16 * wg + (lane & 15)) : -1;
+                my_j_next = entry(i + 1, row);
             }
 
             // ---- softmax of this row, heads h0 .. h0+31
@@ -564,7 +614,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                     if (tmax > m_old + kRescaleThreshold) {
                         alpha = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - tmax);
                         sM[wt] = tmax;
-                        sL[wt] *= alpha;
                         if (i > 0) sFlag[1] = 1;
                     }
                     sAlpha[wt] = alpha;
@@ -572,12 +621,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 named_sync_all_workers();
                 const bool rescale = sFlag[1] != 0;
                 if (rescale) {
-                    // O^T *= alpha per head; PV of the previous tile has completed
+                    // O^T and the running sums *= alpha per head; PV of the previous
+                    // tile has completed (both of its chunk barriers were waited above)
                     float al[32];
 #pragma unroll
                     for (int h4 = 0; h4 < 8; ++h4) {
                         const float4 a4 = reinterpret_cast<const float4 *>(sAlpha + h0)[h4];
                         al[4 * h4] = a4.x; al[4 * h4 + 1] = a4.y; al[4 * h4 + 2] = a4.z; al[4 * h4 + 3] = a4.w;
+                    }
+                    {
+                        float o[32];
+                        tmem_ld32(tL, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) o[h] *= al[h];
+                        tmem_st32(tL, o);
                     }
 #pragma unroll 1
                     for (int mb = 0; mb < 4; ++mb) {
@@ -617,27 +675,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p);
-            int my_j_next = -1;
-            if (more) {
-                load_chunk(i + 1, 2);
-                load_chunk(i + 1, 3);
-                if (i + 2 < n_tiles) gj = lane < 16 ? entry(i + 2, 16 * wg + sub) : -1;
-                my_j_next = entry(i + 1, row);
+            {
+                float o[32];
+                tmem_ld32(tL, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < 32; ++h) o[h] += x[h];
+                tmem_st32(tL, o);
+                tmem_wait_st();
             }
-            // this tile's row sums: over the warp's 32 rows, then the 4 quarters
-            warp_reduce32<false>(x, lane);
-            sRedL[quarter * 64 + h0 + lane] = x[0];
-            named_sync_all_workers();
-            if (wt < 64)
-                sL[wt] += (sRedL[wt] + sRedL[64 + wt]) + (sRedL[128 + wt] + sRedL[192 + wt]);
             my_j = my_j_next;
         }
         if (!ok) *abort_flag = 1;
+        // the running sums: over the warp's 32 rows, then the 4 quarters
+        float lsum[32];
+        tmem_ld32(tL, lsum);
+        tmem_wait_ld();
+        warp_reduce32<false>(lsum, lane);
+        sRedL[quarter * 64 + h0 + lane] = lsum[0];
         named_sync_all_workers();
+        if (wt < 64) sL[wt] = (sRedL[wt] + sRedL[64 + wt]) + (sRedL[128 + wt] + sRedL[192 + wt]);
 
         // ---- epilogue: O^T (unnormalised) of this split
         if (ok && n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[1], (n_tiles - 1) & 1, abort_flag));
             tc_fence_after();
         }
         if (!ok) *abort_flag = 1;
@@ -646,14 +707,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 
     {
         // ---- merge of the cluster's splits.  Every thread of every CTA reaches
-        // each cluster barrier exactly once, whatever happened above.  32-channel
-        // chunk c belongs to CTA c % S; each CTA scales its O^T block by
-        // 2^(m_s - M) / L and stores it into the owner's receive area, block
-        // (c / S) S + sender, which the owner then sums locally.
+        // each cluster barrier exactly once, whatever happened above.  Each CTA
+        // scales its O^T by 2^(m_s - M) / L and writes it to its slot of the
+        // partial-output workspace (L2-resident: a few MB); after a cluster barrier
+        // the CTA that owns 32-channel chunk c (c % S == rank) sums the splits'
+        // chunks in a fixed order and writes the output.
         cg::cluster_group cluster = cg::this_cluster();
         const int S = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
         float *sFac = reinterpret_cast<float *>(sP);          // [split][head]
-        float *sX = reinterpret_cast<float *>(sV);            // receive area (V and Q tiles)
         cluster_wait();              // (arrived at the start) every CTA of the cluster runs
         // this split's reference max and sum go to every CTA's own table (a peer's
         // V, Q and P tiles may still be in use)
@@ -683,6 +744,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
         }
         __syncthreads();
+        // S == 1: the scaled O^T is the output; else this split's slot [64][512]
+        float *dst0 = S == 1 ? p.out + (int64_t)q * H * CSA2_D
+                             : p.part + ((int64_t)q * S + rank) * kHeads * CSA2_D;
         if (warp > 0) {
             const int h0 = 32 * half;
             const bool any = !*abort_flag && n_tiles > 0;
@@ -702,34 +766,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 #pragma unroll
                     for (int h = 0; h < 32; ++h) o[h] = 0.f;
                 }
-                const int c = 4 * mb + (int)quarter;
-                if (S == 1) {
-                    // a single split: its scaled O^T is the output (lane = channel)
-                    float *od = p.out + ((int64_t)q * H + h0) * CSA2_D + 32 * c + lane;
+                // lane = channel: each store of the warp covers 128 contiguous bytes
+                float *od = dst0 + (int64_t)h0 * CSA2_D + 128 * mb + 32 * (int)quarter + lane;
 #pragma unroll
-                    for (int h = 0; h < 32; ++h)
-                        if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
-                    continue;
-                }
-                float *dst = cluster.map_shared_rank(sX, c % S) +
-                             ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
-#pragma unroll
-                for (int h = 0; h < 32; ++h) dst[h * 32] = o[h] * f[h];
+                for (int h = 0; h < 32; ++h)
+                    if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
             }
         }
-        if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
+        if (S > 1) cluster.sync();   // every split's slot is written (S is uniform)
         // chunks rank, rank + S, ...: lane = channel; a warp sums 4 heads per item
-        // (all their loads in flight together)
+        // (all their loads in flight together), splits in a fixed order
         const int n_own = S > 1 ? (16 - rank + S - 1) / S : 0;
+        const float *part_q = p.part + (int64_t)q * S * kHeads * CSA2_D;
         for (int it = warp; it < n_own * 16; it += kTcThreads / 32) {
             const int k = it >> 4, hb = 4 * (it & 15), c = rank + k * S;
             if (hb >= H) continue;
-            const float *src = sX + k * S * kXBlock + hb * 32 + lane;
+            const float *src = part_q + (int64_t)hb * CSA2_D + 32 * c + lane;
             float v[4][kMaxClusterSplits];
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) v[j][s] = (s < S) ? src[s * kXBlock + j * 32] : 0.f;
+                for (int j = 0; j < 4; ++j)
+                    v[j][s] = (s < S && hb + j < H)
+                                  ? __ldcg(src + ((int64_t)s * kHeads + j) * CSA2_D) : 0.f;
             float *od = p.out + ((int64_t)q * H + hb) * CSA2_D + 32 * c + lane;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -749,10 +808,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
-    // receive area: ceil(16 / S) chunk slots x S senders blocks, largest at S = 7 (21)
-    static_assert(21 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
     static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
-    if (p.splits < 1 || p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
+    if (p.splits < 1 || p.splits > kMaxClusterSplits || (p.splits > 1 && p.part == nullptr))
+        return cudaErrorInvalidValue;
     const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
                         kMaxClusterSplits * 2 * 64 * 4 + 9 * 8 + 64;
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

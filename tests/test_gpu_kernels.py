@@ -352,7 +352,8 @@ def _topk_gpu(scores_np, nvalid, k, pool=None, ld=None):
 
 
 @pytest.mark.parametrize("n,k", [(1, 1), (100, 7), (4096, 64), (4097, 4096), (70001, 2048),
-                                 (300, 2048), (16384, 2048)])
+                                 (73728, 4096), (73729, 2048), (20000, 5000), (300, 2048),
+                                 (16384, 2048)])
 def test_topk_bit_exact(n, k):
     rng = np.random.default_rng(n + k)
     s = rng.normal(size=(3, n)).astype(np.float32)
@@ -365,6 +366,20 @@ def test_topk_bit_exact(n, k):
         ref = O.topk(s[i, :nvalid[i]], k)
         assert cnt[i] == len(ref)
         assert np.array_equal(idx[i, :cnt[i]], ref), i
+
+
+@pytest.mark.parametrize("n", [50000, 65536])
+def test_topk_all_equal_and_few_distinct(n):
+    # every score equal (the k lowest positions win), and scores drawn from 3
+    # values: tens of thousands of keys share every prefix of the radix rounds
+    k = 2048
+    s = np.full((2, n), 1.5, np.float32)
+    rng = np.random.default_rng(n)
+    s[1] = rng.choice(np.array([0.25, 1.0, 3.0], np.float32), size=n)
+    idx, cnt = _topk_gpu(s, [n, n - 1], k)
+    for i, nv in enumerate([n, n - 1]):
+        ref = O.topk(s[i, :nv], k)
+        assert cnt[i] == k and np.array_equal(idx[i, :k], ref), i
 
 
 def test_topk_with_pool_map():
