@@ -38,23 +38,6 @@ constexpr int kIdxThreadsMax = kIdxThreadsGrouped;
 constexpr int kTile = 128;
 constexpr int kEpiBatch = 4;          // tiles the epilogue takes per pass (decode)
 constexpr int kMaxGroupCols = 256;     // group * h_idx (the MMA's N) is at most 256
-constexpr int kHistBins = 2048;        // top-11-bit histogram of the score keys (decode)
-
-// One atomic increment per distinct bin among the warp's lanes (bin ~0u:
-// nothing); a warp's scores are neighbouring entries, whose keys fall in few
-// bins, so the loop is short.
-__device__ __forceinline__ void warp_hist_add(uint32_t *h, uint32_t bin, int lane)
-{
-    unsigned pend = __ballot_sync(0xffffffffu, bin != 0xFFFFFFFFu);
-    while (pend) {
-        const int src = __ffs(pend) - 1;
-        const uint32_t b = __shfl_sync(0xffffffffu, bin, src);
-        const unsigned m = __ballot_sync(0xffffffffu, bin == b);
-        if (lane == src) atomicAdd(h + b, (uint32_t)__popc(m));
-        pend &= ~m;
-    }
-}
-
 // the epilogue warps (2 ..) only
 template <int kEpiThreads>
 __device__ __forceinline__ void named_sync_epilogue()
@@ -87,9 +70,6 @@ struct IndexParams {
     int64_t ld_bm;
     int32_t *n_valid;
     uint32_t *counters;
-    // decode (group 1) only, nullable: per-query histogram of the top 11 bits of
-    // the score keys (the first radix digit of the top-k that follows) [nq][2048]
-    uint32_t *hist0;
 };
 
 // Byte offset of (row r, byte c) in a K-major tile with `rowb`-byte rows under
@@ -144,9 +124,6 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
         if (s_bad) count_event(p.counters, CSA2_CNT_BAD_INPUT);
         p.gtiles[g] = s_bad ? 0 : (s_maxn + kTile - 1) / kTile;
     }
-    if (p.hist0 != nullptr)
-        for (int i = threadIdx.x; i < p.group * kHistBins; i += blockDim.x)
-            p.hist0[(int64_t)q0 * kHistBins + i] = 0u;
     // FP8 query rows: row r = (query in group) * h_idx + head; padding rows = 0
     uint8_t *img = p.q8img + (int64_t)g * p.n_pad * p.d_idx;
     for (int r = warp; r < p.n_pad; r += blockDim.x / 32) {
@@ -378,6 +355,7 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
             uint32_t buse[2] = {0, 0};
             int64_t n_issued = 0;
             int b = 0, pn = 0;
+            const uint64_t l2_once = l2_evict_first_policy();
             int64_t base = 0, room = 0;
             // Reindex: lane i's pool block of the tiles 0..3 ahead, loaded 4 tiles
             // early so that these dependent reads overlap (rotated each tile)
@@ -424,8 +402,15 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
                         int64_t nk = p.cap - r0;
                         nk = nk > kTile ? kTile : nk;               // cap % 8 == 0, r0 % 8 == 0
                         mbar_arrive_expect_tx(&full[stage], kABytes + (uint32_t)nk * 4u);
-                        tma_load_2d(dstA, &tmap, 0, (int32_t)r0, &full[stage]);
-                        bulk_load(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage]);
+                        if (kTwoPerSm) {
+                            // query groups re-read the key tiles: default L2 policy
+                            tma_load_2d(dstA, &tmap, 0, (int32_t)r0, &full[stage]);
+                            bulk_load(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage]);
+                        } else {
+                            // decode streams each key once: evict it first, keep the scores
+                            tma_load_2d_hint(dstA, &tmap, 0, (int32_t)r0, &full[stage], l2_once);
+                            bulk_load_hint(dstK, p.kscale + r0, (uint32_t)nk * 4u, &full[stage], l2_once);
+                        }
                     }
                 } else {
                     const int nblk = (pn + 7) / 8;
@@ -445,8 +430,8 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
                     __syncwarp();
                     if (ok_blk) {
                         const int64_t r = base + 8LL * blk;
-                        tma_load_2d(dstA + lane * 8 * D_IDX, &tmap, 0, (int32_t)r, &full[stage]);
-                        bulk_load(dstK + lane * 8, p.kscale + r, 32u, &full[stage]);
+                        tma_load_2d_hint(dstA + lane * 8 * D_IDX, &tmap, 0, (int32_t)r, &full[stage], l2_once);
+                        bulk_load_hint(dstK + lane * 8, p.kscale + r, 32u, &full[stage], l2_once);
                     }
                 }
                 ++n_issued;
@@ -540,9 +525,6 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
         int prev_g = -1;
         float wsr[16];
         int ntq = 0;
-        // the top-k's first histogram, counted straight into the query's global row
-        // (warp-aggregated atomics; no barrier between the epilogue warps)
-        const bool do_hist = !kTwoPerSm && p.hist0 != nullptr && p.group == 1;
         while (it.u < it.u1) {
             const int g = it.g, t = it.t;
             const int q0 = g * p.group;
@@ -604,9 +586,6 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
                         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                         if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q0 * p.ld_bm + (j >> 3)] = bm;
                     }
-                    if (do_hist)
-                        warp_hist_add(p.hist0 + (int64_t)q0 * kHistBins,
-                                      valid ? (score_key(sc) >> 21) : 0xFFFFFFFFu, lane);
                 }
                 // this warp is done with the stages' key scales: its share of their release
                 __syncwarp();
@@ -743,10 +722,9 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
                          const float *w, int h_idx, int64_t max_n, const int32_t *pool_blk,
                          const int32_t *pool_n, int pool_blocks, float *scores, int64_t ld,
                          float *blockmax, int64_t ld_bm, int32_t *n_valid, void *ws,
-                         uint32_t *counters, uint32_t *hist0, cudaStream_t st)
+                         uint32_t *counters, cudaStream_t st)
 {
     IndexParams p{};
-    p.hist0 = qs.group == 1 ? hist0 : nullptr;
     p.kscale = c.kscale;
     p.seq_base = c.seq_base;
     p.seq_len = c.seq_len;

@@ -50,7 +50,6 @@ struct TopkParams {
     TopkState *state;           // [nq]
     uint32_t *ccount;           // [nq][n_chunks][2]  (gt, eq)
     uint32_t *coff;             // [nq][n_chunks][2]  (out offset, eq before)
-    const uint32_t *hist0;      // [nq][kBins] first-round histogram from the indexer, or null
 };
 
 __device__ __forceinline__ int round_shift(int r) { return r == 0 ? 21 : (r == 1 ? 10 : 0); }
@@ -539,318 +538,6 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     }
 }
 
-// ---------------------------------------------------------------- one CTA per query
-// Up to kSelMaxN candidates and k <= kSelMaxK (decode Full layers up to 72K
-// entries, Reindex pools, pools of contexts up to 576K): one CTA of 1024
-// threads per query and only block barriers.  The top 16 bits of every key
-// are kept in shared memory in position order (one padded run per thread).
-//   round 0: histogram of the top 11 bits, built while loading (warp-aggregated
-//            shared atomics) -> bin d0 holding the k-th key;
-//   round 1: the next 5 bits of the keys in bin d0 -> 16-bit prefix P;
-//   keys above P are taken (fewer than k); the candidates (top 16 bits == P)
-//   are listed in position order with their full keys re-read from the score
-//   row, and two 8-bit rounds over them give the exact k-th key T;
-//   the taken candidates (> T, then the lowest-position ties == T) and the
-//   keys above P are two ascending lists, merged into the output.
-// When more than kSelCand candidates share the prefix (heavy ties), the two
-// last rounds and the candidate selection read the candidates' keys from the
-// score row in passes over all positions instead of a list.
-constexpr int kSelThreads = 1024;
-constexpr int kSelMaxRun = 72;                        // keys per thread
-constexpr int kSelMaxN = kSelThreads * kSelMaxRun;    // 73,728
-constexpr int kSelMaxK = 4096;
-constexpr int kSelCand = 4096;
-
-// Block-wide exclusive scan of one 64-bit value per thread (1024 threads).
-__device__ __forceinline__ uint64_t scan_sel(uint64_t v, uint64_t *s_warp, uint64_t *total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint64_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        uint64_t w = s_warp[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        s_warp[lane] = w;                                  // inclusive warp totals
-    }
-    __syncthreads();
-    const uint64_t before = warp > 0 ? s_warp[warp - 1] : 0ull;
-    if (total) *total = s_warp[31];
-    __syncthreads();
-    return before + x - v;
-}
-
-// Digit of a round: bins `nb` (descending from nb - 1), counts in h; the digit
-// d has count(> d) < need <= count(>= d).  Every thread returns d and count(> d).
-__device__ __forceinline__ void pick_digit(const uint32_t *h, int nb, uint32_t need,
-                                           uint64_t *s_warp, uint32_t *s_res, uint32_t &d,
-                                           uint32_t &above)
-{
-    const int per = (nb + kSelThreads - 1) / kSelThreads;    // 1 or 2
-    uint32_t c[2] = {0u, 0u}, mine = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int b = nb - 1 - (threadIdx.x * per + i);
-        if (i < per && b >= 0) c[i] = h[b];
-        mine += c[i];
-    }
-    if (threadIdx.x == 0) { s_res[0] = 0u; s_res[1] = 0u; }
-    const uint32_t before = (uint32_t)scan_sel(mine, s_warp, nullptr);
-    if (before < need && need <= before + mine) {
-        uint32_t acc = before;
-        for (int i = 0; i < per; ++i) {
-            if (need <= acc + c[i]) {
-                s_res[0] = (uint32_t)(nb - 1 - (threadIdx.x * per + i));
-                s_res[1] = acc;
-                break;
-            }
-            acc += c[i];
-        }
-    }
-    __syncthreads();
-    d = s_res[0];
-    above = s_res[1];
-    __syncthreads();
-}
-
-// One shared-memory increment per distinct bin among the warp's lanes (bin
-// ~0u: none): a loop over the distinct bins, free when no lane has one.
-__device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin)
-{
-    unsigned pend = __ballot_sync(0xffffffffu, bin != 0xFFFFFFFFu);
-    while (pend) {
-        const int src = __ffs(pend) - 1;
-        const uint32_t b = __shfl_sync(0xffffffffu, bin, src);
-        const unsigned m = __ballot_sync(0xffffffffu, bin == b);
-        if ((int)(threadIdx.x & 31) == src) atomicAdd(h + b, (uint32_t)__popc(m));
-        pend &= ~m;
-    }
-}
-
-__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkParams p, int run)
-{
-    pdl_wait();
-    pdl_trigger();
-    extern __shared__ __align__(16) uint8_t sel_smem[];
-    const int q = blockIdx.x, tid = threadIdx.x;
-    const int stride = 2 * run + 16;                  // bytes per thread run (padded: bank spread)
-    uint8_t *sK16 = sel_smem;                         // [1024][stride] top 16 key bits
-    int32_t *sA = reinterpret_cast<int32_t *>(sel_smem + (size_t)kSelThreads * stride);   // taken keys
-    int32_t *sCpos = sA + kSelMaxK;                   // candidates: positions
-    uint32_t *sCkey = reinterpret_cast<uint32_t *>(sCpos + kSelCand);                     // and keys
-    __shared__ uint32_t hist[kBins];
-    __shared__ uint64_t s_warp[kSelThreads / 32];
-    __shared__ uint32_t s_res[2];
-
-    int n = p.n_valid[q];
-    if (p.n_div8) n = (n + 7) / 8;
-    if (n < 0) n = 0;
-    if (n > p.max_n) n = (int)p.max_n;
-    const float *row = p.scores + (int64_t)q * p.ld;
-    int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
-    const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
-    auto pos_of = [&](int i) { return pb ? 8 * __ldg(pb + (i >> 3)) + (i & 7) : i; };
-    if (n <= p.k) {
-        for (int i = tid; i < n; i += kSelThreads) out[i] = pos_of(i);
-        if (tid == 0) p.cnt_out[q] = n;
-        return;
-    }
-    if (tid == 0) p.cnt_out[q] = p.k;
-    auto k16_at = [&](int i) -> uint16_t & {
-        return *reinterpret_cast<uint16_t *>(sK16 + (i / run) * stride + 2 * (i % run));
-    };
-    // round-0 histogram: the indexer's count, or built below while loading
-    const bool own_hist = p.hist0 == nullptr;
-    for (int i = tid; i < kBins; i += kSelThreads)
-        hist[i] = own_hist ? 0u : __ldcg(p.hist0 + (int64_t)q * kBins + i);
-    __syncthreads();
-
-    // ---- load (4 consecutive scores per thread and step), top 16 bits to shared
-    // memory, round-0 histogram of the top 11 bits
-    const int n_pad = kSelThreads * run;
-    for (int i0 = 4 * tid; i0 < n_pad; i0 += 4 * kSelThreads) {
-        uint32_t kk[4];
-        if (i0 + 4 <= n) {
-            const float4 f = *reinterpret_cast<const float4 *>(row + i0);
-            kk[0] = score_key(f.x); kk[1] = score_key(f.y);
-            kk[2] = score_key(f.z); kk[3] = score_key(f.w);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) kk[j] = (i0 + j < n) ? score_key(row[i0 + j]) : 0u;
-        }
-        *reinterpret_cast<uint2 *>(&k16_at(i0)) =
-            make_uint2((kk[0] >> 16) | (kk[1] & 0xFFFF0000u), (kk[2] >> 16) | (kk[3] & 0xFFFF0000u));
-        if (own_hist) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) hist_add(hist, (i0 + j < n) ? (kk[j] >> 21) : 0xFFFFFFFFu);
-        }
-    }
-    __syncthreads();
-    uint32_t d0, above0;
-    pick_digit(hist, kBins, (uint32_t)p.k, s_warp, s_res, d0, above0);
-    uint32_t k_rem = (uint32_t)p.k - above0;
-
-    // ---- round 1: bits 16..20 of the keys in bin d0
-    if (tid < 32) hist[tid] = 0u;
-    __syncthreads();
-    for (int i0 = tid; i0 < n_pad; i0 += kSelThreads) {
-        const uint32_t k16 = k16_at(i0);
-        hist_add(hist, (i0 < n && (k16 >> 5) == d0) ? (k16 & 31u) : 0xFFFFFFFFu);
-    }
-    __syncthreads();
-    uint32_t d1, above1;
-    pick_digit(hist, 32, k_rem, s_warp, s_res, d1, above1);
-    k_rem -= above1;
-    const uint32_t P = (d0 << 5) | d1;
-
-    // ---- ordered pass over this thread's run: keys above P are taken (list sA),
-    // keys equal to P are candidates (list sCpos)
-    const int r0 = tid * run;
-    const int nv = run / 8;
-    auto run_vec = [&](int v) {
-        return *reinterpret_cast<const uint4 *>(sK16 + tid * stride + 16 * v);
-    };
-    uint32_t na = 0, nc = 0;
-    for (int v = 0; v < nv; ++v) {
-        const uint4 w = run_vec(v);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = r0 + 8 * v + e;
-            const uint32_t k16 = (ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-            na += (i < n && k16 > P);
-            nc += (i < n && k16 == P);
-        }
-    }
-    uint64_t tot;
-    const uint64_t pre = scan_sel(((uint64_t)na << 32) | nc, s_warp, &tot);
-    const uint32_t NA = (uint32_t)(tot >> 32), NC = (uint32_t)tot;
-    {
-        uint32_t oa = (uint32_t)(pre >> 32), oc = (uint32_t)pre;
-        for (int v = 0; v < nv; ++v) {
-            const uint4 w = run_vec(v);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = r0 + 8 * v + e;
-                const uint32_t k16 = (ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-                if (i < n && k16 > P) sA[oa++] = i;
-                if (i < n && k16 == P) {
-                    if (oc < (uint32_t)kSelCand) sCpos[oc] = i;
-                    ++oc;
-                }
-            }
-        }
-    }
-    __syncthreads();
-    const bool listed = NC <= (uint32_t)kSelCand;
-    if (listed)
-        for (uint32_t c = tid; c < NC; c += kSelThreads) sCkey[c] = score_key(row[sCpos[c]]);
-    // the candidates' full keys, from the list or from the score row
-    auto cand_key = [&](int i) { return score_key(row[i]); };
-
-    // ---- rounds 2, 3: bits 8..15, then 0..7, of the candidates' keys
-    uint32_t T = P << 16;
-    for (int r = 0; r < 2; ++r) {
-        const int sh = r == 0 ? 8 : 0;
-        if (tid < 256) hist[tid] = 0u;
-        __syncthreads();
-        const uint32_t match_sh = r == 0 ? 16u : 8u;           // key bits fixed so far
-        const uint32_t match = T >> match_sh;
-        if (listed) {
-            for (uint32_t c0 = 0; c0 < NC; c0 += kSelThreads) {
-                const uint32_t c = c0 + tid;
-                const uint32_t key = c < NC ? sCkey[c] : 0u;
-                hist_add(hist, (c < NC && (key >> match_sh) == match) ? ((key >> sh) & 255u) : 0xFFFFFFFFu);
-            }
-        } else {
-            for (int i0 = tid; i0 < n_pad; i0 += kSelThreads) {
-                uint32_t bin = 0xFFFFFFFFu;
-                if (i0 < n && k16_at(i0) == P) {
-                    const uint32_t key = cand_key(i0);
-                    if ((key >> match_sh) == match) bin = (key >> sh) & 255u;
-                }
-                hist_add(hist, bin);
-            }
-        }
-        __syncthreads();
-        uint32_t d, above;
-        pick_digit(hist, 256, k_rem, s_warp, s_res, d, above);
-        k_rem -= above;
-        T |= d << sh;
-    }
-    // k_rem = candidates equal to T that are taken (the lowest positions)
-
-    // ---- the taken candidates, ascending: key > T, or key == T within the first k_rem
-    int32_t *sSel = listed ? reinterpret_cast<int32_t *>(sel_smem)          // (runs no longer read)
-                           : reinterpret_cast<int32_t *>(sCkey);
-    if (listed) {
-        const int cr = (NC + kSelThreads - 1) / kSelThreads;
-        const int c0 = tid * cr, c1 = min((int)NC, c0 + cr);
-        uint32_t eq = 0;
-        for (int c = c0; c < c1; ++c) eq += sCkey[c] == T;
-        const uint32_t eq_before = (uint32_t)scan_sel(eq, s_warp, nullptr);
-        uint32_t ns = 0, er = eq_before;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t key = sCkey[c];
-            ns += key > T || (key == T && er < k_rem);
-            er += key == T;
-        }
-        uint32_t o = (uint32_t)scan_sel(ns, s_warp, nullptr);
-        er = eq_before;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t key = sCkey[c];
-            if (key > T || (key == T && er < k_rem)) sSel[o++] = sCpos[c];
-            er += key == T;
-        }
-    } else {
-        uint32_t eq = 0;
-        for (int i = r0; i < r0 + run; ++i)
-            if (i < n && k16_at(i) == P) eq += cand_key(i) == T;
-        const uint32_t eq_before = (uint32_t)scan_sel(eq, s_warp, nullptr);
-        uint32_t ns = 0, er = eq_before;
-        for (int i = r0; i < r0 + run; ++i) {
-            if (i < n && k16_at(i) == P) {
-                const uint32_t key = cand_key(i);
-                ns += key > T || (key == T && er < k_rem);
-                er += key == T;
-            }
-        }
-        uint32_t o = (uint32_t)scan_sel(ns, s_warp, nullptr);
-        er = eq_before;
-        for (int i = r0; i < r0 + run; ++i) {
-            if (i < n && k16_at(i) == P) {
-                const uint32_t key = cand_key(i);
-                if (key > T || (key == T && er < k_rem)) sSel[o++] = i;
-                er += key == T;
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- merge of the two ascending lists (positions are distinct)
-    const int NS = p.k - (int)NA;
-    auto lower = [](const int32_t *a, int len, int x) {
-        int lo = 0, hi = len;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (a[mid] < x) lo = mid + 1; else hi = mid;
-        }
-        return lo;
-    };
-    for (int i = tid; i < (int)NA; i += kSelThreads) out[i + lower(sSel, NS, sA[i])] = pos_of(sA[i]);
-    for (int j = tid; j < NS; j += kSelThreads) out[j + lower(sA, (int)NA, sSel[j])] = pos_of(sSel[j]);
-}
-
 // Pool size: 8 per chosen block, minus the invisible tail of the newest block
 // when it is partial and was chosen.
 __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
@@ -885,10 +572,9 @@ size_t topk_workspace_bytes(int nq, int64_t max_n)
 cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid, int n_div8,
                         const int32_t *pool_blk, int pool_blocks, int nq, int64_t max_n, int k,
                         int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out, void *ws,
-                        const uint32_t *hist0, cudaStream_t st)
+                        cudaStream_t st)
 {
     TopkParams p{};
-    p.hist0 = hist0;
     p.scores = scores;
     p.ld = ld;
     p.n_valid = n_valid;
@@ -913,15 +599,6 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     w += align_up((size_t)nq * ws_chunks * 8, 256);
     p.coff = reinterpret_cast<uint32_t *>(w);
 
-    if (hist0 != nullptr && topk_select_fits(max_n, k)) {
-        // runs of a multiple of 8 keys per thread (16-byte shared reads)
-        const int run = (int)(((max_n + kSelThreads - 1) / kSelThreads + 7) & ~7);
-        const size_t smem = (size_t)kSelThreads * (2 * run + 16) + (size_t)(kSelMaxK + 2 * kSelCand) * 4;
-        cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const cudaError_t e = launch_k(topk_select_kernel, dim3(nq), dim3(kSelThreads), smem, st, 0,
-                                       p, run);
-        return e != cudaSuccess ? e : cudaGetLastError();
-    }
     if (max_n <= kClusterMax) {
         const int chunk = (int)(((max_n + kClusterCtas - 1) / kClusterCtas + 3) & ~3);
         const size_t smem = (size_t)chunk * 4;
@@ -944,8 +621,6 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-bool topk_select_fits(int64_t max_n, int k) { return max_n <= kSelMaxN && k <= kSelMaxK; }
-
 cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_valid, int nq,
                         int64_t max_n, int pool_blocks, int32_t *pool_blk, int32_t *pool_n,
                         void *ws, cudaStream_t st)
@@ -953,7 +628,7 @@ cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_v
     // the counts of chosen blocks go to pool_n first, then become positions
     const int64_t max_blocks = (max_n + 7) / 8;
     cudaError_t e = launch_topk(blockmax, ld_bm, n_valid, 1, nullptr, 0, nq, max_blocks,
-                                pool_blocks, pool_blk, pool_blocks, pool_n, ws, nullptr, st);
+                                pool_blocks, pool_blk, pool_blocks, pool_n, ws, st);
     if (e != cudaSuccess) return e;
     e = launch_k(pool_count_kernel, dim3((nq + 127) / 128), dim3(128), 0, st, 0,
                  (const int32_t *)n_valid, (const int32_t *)pool_blk, pool_blocks,
@@ -1019,7 +694,7 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t ld_scores,
     if (scratch == nullptr) return CSA2_ERR_CUDA;
     // launch_topk's first kernel clears the histograms and state it reads later
     const cudaError_t e = launch_topk(scores, ld_scores, n_valid, 0, pool_blk, pool_blocks, nq,
-                                      max_n, k, idx_out, ld_idx, cnt_out, scratch, nullptr,
+                                      max_n, k, idx_out, ld_idx, cnt_out, scratch,
                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
