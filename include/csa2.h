@@ -252,11 +252,9 @@ csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const i
  * outside the contract); the softmax weights P are stored as f16 (at most 256
  * before normalisation, relative error 2^-11).  Logits, the softmax and every
  * sum are fp32.
- * Workspace: a query's row tiles are divided over at most 8 CTAs of one
- * thread-block cluster when there are fewer queries than SMs; each CTA writes
- * its scaled partial output (64 x 512 fp32) to the workspace and the cluster
- * sums them.  csa2_attn_workspace_size() gives the bytes for the current
- * device (0 when every query is one CTA; then the argument may be NULL). */
+ * The attention needs no workspace (csa2_attn_workspace_size() is 0; the
+ * argument may be NULL): a query's row tiles are divided over at most 8 CTAs
+ * of one thread-block cluster, which merge on chip. */
 csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *queries,
                              const int32_t *idx, int64_t ld_idx, const int32_t *cnt,
                              int32_t k_max, const uint16_t *q, int32_t H, const uint16_t *win,

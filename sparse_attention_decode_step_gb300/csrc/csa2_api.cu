@@ -80,14 +80,12 @@ int attn_plan(int nq, int k_max, int n_win)
     return s;
 }
 
-// A query split over several CTAs merges through a workspace slot per split
-// (its scaled partial output, [64 heads][512] fp32); a query that is one CTA
-// writes its output directly.
+// The splits of a query merge on chip (distributed shared memory): the
+// attention needs no workspace.
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win)
 {
-    (void)H;
-    const int s = attn_plan(nq, k_max, n_win);
-    return s > 1 ? (size_t)nq * s * 64 * CSA2_D * sizeof(float) : 0;
+    (void)nq; (void)H; (void)k_max; (void)n_win;
+    return 0;
 }
 
 }  // namespace csa2
@@ -355,10 +353,7 @@ csa2_status sparse_attn_impl(const csa2_cache *cache, const csa2_queries *querie
                      (cnt == nullptr || al4(cnt)) && (win == nullptr || al16(win)) &&
                      (win_start == nullptr || al4(win_start)) && (lse == nullptr || al4(lse)),
                  CSA2_ERR_ALIGN);
-    const size_t need = attn_workspace_bytes(queries->nq, H, k_max, n_win);
-    CSA2_REQUIRE(ws_bytes >= need, CSA2_ERR_CAPACITY);
-    CSA2_REQUIRE(need == 0 || (workspace != nullptr && al16(workspace)),
-                 workspace == nullptr ? CSA2_ERR_INVALID_ARG : CSA2_ERR_ALIGN);
+    CSA2_REQUIRE(ws_bytes >= attn_workspace_bytes(queries->nq, H, k_max, n_win), CSA2_ERR_CAPACITY);
     AttnParams p{};
     p.codes = cache->codes;
     p.scales = cache->scales;
@@ -383,7 +378,7 @@ csa2_status sparse_attn_impl(const csa2_cache *cache, const csa2_queries *querie
     p.out = out;
     p.lse = lse;
     p.splits = attn_plan(p.nq, k_max, n_win);
-    p.part = need > 0 ? static_cast<float *>(workspace) : nullptr;
+    (void)workspace;
     p.counters = counters;
     p.early = early;
     return cuda_status(launch_attn_tc(p, static_cast<cudaStream_t>(stream)));

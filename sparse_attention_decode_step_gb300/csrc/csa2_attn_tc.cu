@@ -28,17 +28,17 @@
 // releases chunk 0 of the V tile after its first two channel blocks, so the
 // workers store chunk 0 of tile i + 1 while PV finishes, and the QK product of
 // tile i + 1 over chunk 0 runs while chunk 1 is stored.  The next tile's codes
-// are loaded as soon as this tile's chunks are stored (during the QK product
-// and the softmax); the rows of the tile after that are asked of L2 one tile
-// earlier.  In the softmax a worker owns half of a tile row (32 heads), two per
+// are loaded in two halves, chunk 0 while this tile's QK product finishes and
+// chunk 1 once its P is stored (while its PV product starts); the rows of the
+// tile after that are asked of L2 one tile earlier.  In the softmax a worker owns half of a tile row (32 heads), two per
 // TMEM lane quarter.  The cross-row max reduction runs only when a logit
 // exceeds its head's reference max by more than 8 (always on the first tile);
 // each thread keeps its rows' sums and they are reduced once, at the end.  The
 // splits of a query (at most 8) form a thread-block cluster: every CTA sends
-// its reference max and sum to all peers through distributed shared memory,
-// writes its O^T scaled by 2^(m_s - M) / L to its slot of a workspace (L2),
-// and after a cluster barrier the CTA that owns a 32-channel chunk sums the
-// splits' slots for it and writes the output.  The set-up that reads nothing
+// its reference max and sum to all peers, scales its O^T by 2^(m_s - M) / L
+// and stores each 32-channel chunk into the shared memory of the CTA that owns
+// the chunk, which sums the splits' chunks and writes the output.  Nothing
+// goes through global memory between splits.  The set-up that reads nothing
 // the previous kernel writes (barriers, TMEM, and inside a layer step the
 // query block) runs before the programmatic-dependent-launch wait.
 #include <cooperative_groups.h>
@@ -257,6 +257,10 @@ __device__ __forceinline__ void named_sync_all_workers()
     asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// Cluster merge: a block of the receive area is one 32-channel chunk of one
+// split, [64 heads][32 channels] fp32 (8 KB), so that a warp (lane = channel)
+// writes and reads 128 contiguous bytes per head.
+constexpr int kXBlock = 64 * 32;
 constexpr int kMaxClusterSplits = 8;
 
 __device__ __forceinline__ void cluster_arrive()
@@ -368,11 +372,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         const int g = tile_row(tile, r);
         return (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
     };
-    auto load_tile = [&](int tile) {
-        gkind = 0;
+    // the register slots of channel chunk hc (slots 4 hc .. 4 hc + 3) with tile `tile`
+    auto load_half = [&](int tile, int hc) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 4 * hc; t < 4 * hc + 4; ++t) {
             const int h = t >> 2, x = t & 3;
+            gkind &= ~((1u << t) | (1u << (8 + t)));
             const int rw = 4 * x + (lane >> 3);
             const int g = tile_row(tile, 16 * wg + rw);
             const int j = __shfl_sync(0xffffffffu, gj, rw);
@@ -457,7 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     if (warp > 0 && n_tiles > 0) {
         gj = lane < 16 ? entry(0, 16 * wg + (lane & 15)) : -1;
         my_j = entry(0, row);
-        load_tile(0);
+        load_half(0, 0);
+        load_half(0, 1);
         if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + (lane & 15)) : -1;
         if (n_tiles > 2) gj2 = lane < 16 ? entry(2, 16 * wg + (lane & 15)) : -1;
     }
@@ -565,15 +571,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 if (lane == 0) mbar_arrive(&bar_v[h]);
             }
             if (!ok) break;
-            // the next tile's codes, in flight during the QK product and the softmax
+            // the next tile's codes: chunk 0 while the QK product finishes, chunk 1
+            // (below) while the PV product of this tile starts
             const bool more = i + 1 < n_tiles;
             int my_j_next = -1;
-            if (more) {
-                load_tile(i + 1);
-                gj = gj2;
-                if (i + 3 < n_tiles) gj2 = lane < 16 ? entry(i + 3, 16 * wg + (lane & 15)) : -1;
-                my_j_next = entry(i + 1, row);
-            }
+            if (more) load_half(i + 1, 0);
 
             // ---- softmax of this row, heads h0 .. h0+31
             ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_s, i & 1, abort_flag));
@@ -675,6 +677,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p);
+            if (more) {
+                load_half(i + 1, 1);
+                gj = gj2;
+                if (i + 3 < n_tiles) gj2 = lane < 16 ? entry(i + 3, 16 * wg + (lane & 15)) : -1;
+                my_j_next = entry(i + 1, row);
+            }
             {
                 float o[32];
                 tmem_ld32(tL, o);
@@ -707,14 +715,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 
     {
         // ---- merge of the cluster's splits.  Every thread of every CTA reaches
-        // each cluster barrier exactly once, whatever happened above.  Each CTA
-        // scales its O^T by 2^(m_s - M) / L and writes it to its slot of the
-        // partial-output workspace (L2-resident: a few MB); after a cluster barrier
-        // the CTA that owns 32-channel chunk c (c % S == rank) sums the splits'
-        // chunks in a fixed order and writes the output.
+        // each cluster barrier exactly once, whatever happened above.
         cg::cluster_group cluster = cg::this_cluster();
         const int S = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
         float *sFac = reinterpret_cast<float *>(sP);          // [split][head]
+        float *sX = reinterpret_cast<float *>(sV);            // receive area (V and Q tiles)
         cluster_wait();              // (arrived at the start) every CTA of the cluster runs
         // this split's reference max and sum go to every CTA's own table (a peer's
         // V, Q and P tiles may still be in use)
@@ -744,9 +749,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
         }
         __syncthreads();
-        // S == 1: the scaled O^T is the output; else this split's slot [64][512]
-        float *dst0 = S == 1 ? p.out + (int64_t)q * H * CSA2_D
-                             : p.part + ((int64_t)q * S + rank) * kHeads * CSA2_D;
         if (warp > 0) {
             const int h0 = 32 * half;
             const bool any = !*abort_flag && n_tiles > 0;
@@ -766,29 +768,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 #pragma unroll
                     for (int h = 0; h < 32; ++h) o[h] = 0.f;
                 }
-                // lane = channel: each store of the warp covers 128 contiguous bytes
-                float *od = dst0 + (int64_t)h0 * CSA2_D + 128 * mb + 32 * (int)quarter + lane;
+                const int c = 4 * mb + (int)quarter;
+                if (S == 1) {
+                    // a single split: its scaled O^T is the output (lane = channel)
+                    float *od = p.out + ((int64_t)q * H + h0) * CSA2_D + 32 * c + lane;
 #pragma unroll
-                for (int h = 0; h < 32; ++h)
-                    if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
+                    for (int h = 0; h < 32; ++h)
+                        if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
+                    continue;
+                }
+                float *dst = cluster.map_shared_rank(sX, c % S) +
+                             ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
+#pragma unroll
+                for (int h = 0; h < 32; ++h) dst[h * 32] = o[h] * f[h];
             }
         }
-        if (S > 1) cluster.sync();   // every split's slot is written (S is uniform)
+        if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
         // chunks rank, rank + S, ...: lane = channel; a warp sums 4 heads per item
-        // (all their loads in flight together), splits in a fixed order
+        // (all their loads in flight together)
         const int n_own = S > 1 ? (16 - rank + S - 1) / S : 0;
-        const float *part_q = p.part + (int64_t)q * S * kHeads * CSA2_D;
         for (int it = warp; it < n_own * 16; it += kTcThreads / 32) {
             const int k = it >> 4, hb = 4 * (it & 15), c = rank + k * S;
             if (hb >= H) continue;
-            const float *src = part_q + (int64_t)hb * CSA2_D + 32 * c + lane;
+            const float *src = sX + k * S * kXBlock + hb * 32 + lane;
             float v[4][kMaxClusterSplits];
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    v[j][s] = (s < S && hb + j < H)
-                                  ? __ldcg(src + ((int64_t)s * kHeads + j) * CSA2_D) : 0.f;
+                for (int j = 0; j < 4; ++j) v[j][s] = (s < S) ? src[s * kXBlock + j * 32] : 0.f;
             float *od = p.out + ((int64_t)q * H + hb) * CSA2_D + 32 * c + lane;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -808,9 +815,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
 
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
+    // receive area: ceil(16 / S) chunk slots x S senders blocks, largest at S = 7 (21)
+    static_assert(21 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
     static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
-    if (p.splits < 1 || p.splits > kMaxClusterSplits || (p.splits > 1 && p.part == nullptr))
-        return cudaErrorInvalidValue;
+    if (p.splits < 1 || p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
     const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
                         kMaxClusterSplits * 2 * 64 * 4 + 9 * 8 + 64;
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

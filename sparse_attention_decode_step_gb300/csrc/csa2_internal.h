@@ -99,7 +99,6 @@ struct AttnParams {
     float *out, *lse;
     int splits;         // CTAs per query; its tiles are divided evenly over them
     uint32_t *counters;
-    float *part;        // splits > 1: [nq][splits][64 heads][512] scaled partial outputs
     // 1: q (and the window and the cache) are not written by the kernel launched
     // just before on the stream, so they may be read before the programmatic
     // dependent-launch wait (csa2_layer_step after its own top-k)
