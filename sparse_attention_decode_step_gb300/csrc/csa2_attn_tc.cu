@@ -721,6 +721,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         float *sFac = reinterpret_cast<float *>(sP);          // [split][head]
         float *sX = reinterpret_cast<float *>(sV);            // receive area (V and Q tiles)
         cluster_wait();              // (arrived at the start) every CTA of the cluster runs
+        // the workers' sM and sL are final before the MMA warp (threads 0 .. 31)
+        // reads them: it takes no part in the workers' named barriers
+        __syncthreads();
         // this split's reference max and sum go to every CTA's own table (a peer's
         // V, Q and P tiles may still be in use)
         if (tid < 64) {

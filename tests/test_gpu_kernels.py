@@ -609,3 +609,44 @@ def test_attention_peaky_logits_rescale_and_split_merge(layout):
         err = rel_rows(go[i], ref)
         assert err.max() <= TOL, (i, int(err.argmax()), float(err.max()))
         assert np.abs(gl[i] - rlse).max() <= 1e-3 * max(1.0, np.abs(rlse).max()), i
+
+
+# ---------------------------------------------------------------- layer top-k under heavy ties
+@pytest.mark.parametrize("distinct", [1, 3, 400, 2000])
+def test_layer_full_topk_with_few_distinct_scores(distinct):
+    # Inside csa2_layer_step a decode Full layer's indexer counts the top-k's
+    # first radix digit and a cluster per query selects from it; with every
+    # entry's key one of `distinct` integer vectors, scores tie by the tens of
+    # thousands (1, 3: the threshold bin exceeds the selection's candidate list
+    # and its copy area) or by the tens to hundreds (400, 2000: ties at the k-th
+    # score in both slices of the row), and the lowest positions must win among
+    # equal scores.
+    n_ent, B, k = 40000, 2, 2048
+    wl = ci.Workload("t", B, [n_ent] * B, 0, 1, exact=True, seed=41)
+    cache = csa.Cache([n_ent + 8] * B, wl.d_idx, 1, DEV)
+    g = torch.Generator().manual_seed(41)
+    vecs = torch.randint(-8, 9, (distinct, wl.d_idx), generator=g).float()
+    keys = []
+    for b in range(B):
+        C, _ = ci.latent_rows(wl, b, 0, n_ent, DEV)
+        pick = torch.randint(0, distinct, (n_ent,), generator=g)
+        keys.append(vecs[pick])
+        csa.quantize_append(cache, C[None].contiguous(), None, keys[b][None].contiguous().to(DEV),
+                            seq=b)
+    qi, w, qa = ci.query_inputs(wl, B, "cpu")
+    qs = csa.Queries(list(range(B)), [n_ent - 1] * B, 1, DEV)
+    win = ci.window_rows(wl, B, 256, DEV)
+    idx = torch.full((B, k), -1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(B, dtype=torch.int32, device=DEV)
+    out = torch.zeros(B, wl.heads, 512, device=DEV)
+    counters = csa.new_counters()
+    csa.Layer(csa.FULL, cache, qs, k=k, q=qa.to(DEV), win=win, n_win=wl.n_win, out=out, idx=idx,
+              cnt=cnt, q_idx=qi.to(DEV), w=w.to(DEV), max_n=n_ent, counters=counters)()
+    torch.cuda.synchronize()
+    assert _np(counters).tolist() == [0, 0, 0, 0]
+    for b in range(B):
+        k8, ks = O.fp8_encode_rows(keys[b].numpy())
+        sc = O.scores_full(k8, ks, qi[b].numpy(), w[b].numpy(), 0, n_ent)
+        assert len(np.unique(sc)) <= distinct
+        ref = O.topk(sc, k)
+        assert int(cnt[b]) == k and np.array_equal(_np(idx[b]), ref), b
