@@ -21,26 +21,33 @@
 // more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
 // in TMEM.
 //
-// Warps: 0 = MMA issuer / TMEM owner; 1..8 = workers.  V is gathered with 8
-// lanes per row (128 contiguous code bytes = one 128-byte line per row, 4 rows
-// per warp load) and dequantised in two 256-channel chunks, each with its own
-// barrier.  The chunks are pipelined across tiles: the PV product of tile i
-// releases chunk 0 of the V tile after its first two channel blocks, so the
-// workers store chunk 0 of tile i + 1 while PV finishes, and the QK product of
-// tile i + 1 over chunk 0 runs while chunk 1 is stored.  The next tile's codes
-// are loaded in two halves, chunk 0 while this tile's QK product finishes and
-// chunk 1 once its P is stored (while its PV product starts); the rows of the
-// tile after that are asked of L2 one tile earlier.  In the softmax a worker owns half of a tile row (32 heads), two per
-// TMEM lane quarter.  The cross-row max reduction runs only when a logit
-// exceeds its head's reference max by more than 8 (always on the first tile);
-// each thread keeps its rows' sums and they are reduced once, at the end.  The
+// Warps: 0..15 = workers (warp 0 also owns TMEM), 16 = MMA issuer (the
+// issuing thread stalls while the tensor pipe's queue is full, so it must not
+// hold up the workers).  Sixteen workers keep four warps on each scheduler; a
+// 17-warp CTA gets at most 96 registers per thread.  V is gathered with 8 lanes
+// per row (128 contiguous code bytes = one 128-byte line per row, 4 rows per
+// warp load, 8 rows per warp and tile) and dequantised in two 256-channel
+// chunks, each with its own barrier.  The chunks are pipelined across tiles:
+// the PV product of tile i releases chunk 0 of the V tile after its first two
+// channel blocks, so the workers store chunk 0 of tile i + 1 while PV
+// finishes, and the QK product of tile i + 1 over chunk 0 runs while chunk 1
+// is stored.  The next tile's codes are loaded in two halves, chunk 0 while
+// this tile's QK product finishes and chunk 1 once its P is stored (while its
+// PV product starts); the rows of the tile after that are asked of L2 one tile
+// earlier.  In the softmax a worker owns a quarter of a tile row (16 heads),
+// four per TMEM lane quarter.  The cross-row max reduction runs only when a
+// logit exceeds its head's reference max by more than 8 (always on the first
+// tile); each thread keeps its row's sums in TMEM and they are reduced once,
+// at the end.  The workers' votes and barriers leave the MMA warp out, whose
+// waits are bounded and end when the workers raise the abort flag.  The
 // splits of a query (at most 8) form a thread-block cluster: every CTA sends
 // its reference max and sum to all peers, scales its O^T by 2^(m_s - M) / L
 // and stores each 32-channel chunk into the shared memory of the CTA that owns
 // the chunk, which sums the splits' chunks and writes the output.  Nothing
 // goes through global memory between splits.  The set-up that reads nothing
 // the previous kernel writes (barriers, TMEM, and inside a layer step the
-// query block) runs before the programmatic-dependent-launch wait.
+// query block and the query's metadata) runs before the
+// programmatic-dependent-launch wait.
 #include <cooperative_groups.h>
 
 #include "csa2_device.cuh"
@@ -50,7 +57,7 @@ namespace cg = cooperative_groups;
 
 namespace csa2 {
 
-constexpr int kTcThreads = 288;       // warp 0 MMA, warps 1..8 workers
+constexpr int kTcThreads = 544;       // warps 0..15 workers, warp 16 MMA issuer
 constexpr int kRows = 128;           // rows per tile (MMA M)
 constexpr int kHeads = 64;           // MMA N (heads padded to 64)
 constexpr uint32_t kVBytes = kRows * CSA2_D * 2;          // 128 KB
@@ -63,11 +70,6 @@ constexpr float kRescaleThreshold = 8.0f;                 // log2 units
 __device__ __forceinline__ void fence_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_sync_workers()
-{
-    asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 // 8 E2M1 codes (one 32-bit word, channel 2i in the low nibble of byte i) ->
@@ -123,73 +125,8 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64])
-{
-    uint32_t r[64];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
-          "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
-          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
-          "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
-          "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&v)[64])
-{
-    uint32_t r[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(v[i]);
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
-        "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
-        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]),
-        "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]),
-        "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]),
-        "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]),
-        "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
-{
-    uint32_t r[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
 }
 
 // 2^x (hardware approximation, relative error near 2^-22; 2^-inf = 0)
@@ -200,13 +137,32 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
-// Transposed warp reduction of 32 values per lane: afterwards lane l holds, in
-// v[0], the reduction over the warp's 32 lanes of value l.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// Transposed warp reduction of 16 values per lane: afterwards lanes l and
+// l + 16 hold, in v[0], the reduction over all 32 lanes of value l & 15.
 template <bool kMax>
-__device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane)
+__device__ __forceinline__ void warp_reduce16(float (&v)[16], int lane)
 {
 #pragma unroll
-    for (int n = 32, o = 16; n > 1; n >>= 1, o >>= 1) {
+    for (int i = 0; i < 16; ++i) {
+        const float recv = __shfl_xor_sync(0xffffffffu, v[i], 16);
+        v[i] = kMax ? fmaxf(v[i], recv) : v[i] + recv;
+    }
+#pragma unroll
+    for (int n = 16, o = 8; n > 1; n >>= 1, o >>= 1) {
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < n / 2; ++i) {
@@ -218,7 +174,35 @@ __device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane)
     }
 }
 
-// Row set of one query (selected entries, then window positions).
+constexpr int kWorkerWarps = 16;                     // four per TMEM lane quarter
+constexpr int kWorkers = 32 * kWorkerWarps;
+
+// CTA barrier of the worker warps alone (the MMA warp never takes part)
+__device__ __forceinline__ void workers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+}
+
+// The same barrier, returning whether v holds for every worker thread
+__device__ __forceinline__ bool workers_and(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        ".reg .pred pin, pout;\n"
+        "setp.ne.u32 pin, %1, 0;\n"
+        "bar.red.and.pred pout, 1, %2, pin;\n"
+        "selp.u32 %0, 1, 0, pout;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kWorkers)
+        : "memory");
+    return r != 0;
+}
+
+// Row set of one query (selected entries, then window positions).  The
+// metadata part reads only the caller's query and cache descriptors; the
+// count of selected entries (written by a top-k just before) is read apart.
 struct TcRowSet {
     int b, cnt, nw;
     int64_t base, lo, nt;
@@ -237,8 +221,6 @@ __device__ __forceinline__ TcRowSet tc_row_set(const AttnParams &p, int q)
     const int64_t len = p.seq_len[rs.b];
     if (nt > len) nt = len;
     rs.nt = nt;
-    rs.cnt = (p.cnt != nullptr && p.k_max > 0) ? min(p.cnt[q], p.k_max) : 0;
-    if (rs.cnt < 0) rs.cnt = 0;
     if (p.win != nullptr && p.n_win > 0 && t >= 0) {
         int64_t lo = t - p.n_win + 1;
         const int64_t s = p.win_start ? (int64_t)p.win_start[rs.b] : 0;
@@ -250,11 +232,10 @@ __device__ __forceinline__ TcRowSet tc_row_set(const AttnParams &p, int q)
     return rs;
 }
 
-constexpr int kWorkers = 256;                        // 8 worker warps, two per TMEM lane quarter
-
-__device__ __forceinline__ void named_sync_all_workers()
+__device__ __forceinline__ int tc_row_count(const AttnParams &p, int q)
 {
-    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const int c = (p.cnt != nullptr && p.k_max > 0) ? min(p.cnt[q], p.k_max) : 0;
+    return c < 0 ? 0 : c;
 }
 
 // Cluster merge: a block of the receive area is one 32-channel chunk of one
@@ -293,22 +274,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     float *sML = sRedL + 4 * 64;              // cluster merge: [split][m | l][64 heads]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sML + kMaxClusterSplits * 2 * 64);
     uint64_t *bar_v = bars;                   // [2]: V channel chunk h (256 channels) stored
-    uint64_t *bar_s = bars + 2, *bar_p = bars + 3;
-    uint64_t *bar_o = bars + 4;               // [2]: PV channel blocks 2h, 2h + 1 done
+    uint64_t *bar_o = bars + 2;               // [2]: PV channel blocks 2h, 2h + 1 done (chunk h free)
+    uint64_t *bar_s = bars + 4, *bar_p = bars + 5;   // S^T complete; P stored
     uint64_t *bar_done = bars + 6, *bar_q = bars + 7;
-    int *sFlag = reinterpret_cast<int *>(bars + 9);   // [0] abort [1] rescale [2] bad [3] need max
+    int *sFlag = reinterpret_cast<int *>(bars + 8);   // [0] abort [1] rescale [2] bad [3] need max
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sFlag + 4);
     volatile int *abort_flag = sFlag;
 
     // ---- set-up that reads nothing an earlier kernel writes: barriers, TMEM, and
-    // (p.early) the query block, whose bulk copy lands in the still-free V tile
+    // (p.early) the query block, whose bulk copy lands in the still-free V tile,
+    // and the query's row-set metadata
     if (tid == 0) {
         for (int c = 0; c < 2; ++c) {
-            mbar_init(&bar_v[c], kWorkers / 32);
+            mbar_init(&bar_v[c], kWorkerWarps);
             mbar_init(&bar_o[c], 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, kWorkers / 32);
+        mbar_init(bar_p, kWorkerWarps);
         mbar_init(bar_done, 1);
         mbar_init(bar_q, 1);
         sFlag[0] = 0;
@@ -329,11 +311,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     };
     if (tid == 0 && p.early) load_q();
     if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
+    TcRowSet rs{};
+    if (p.early) rs = tc_row_set(p, q);
     pdl_wait();
     pdl_trigger();
     if (tid == 0 && !p.early) load_q();
-
-    const TcRowSet rs = tc_row_set(p, q);
+    if (!p.early) rs = tc_row_set(p, q);
+    if (!rs.bad) rs.cnt = tc_row_count(p, q);
     if (tid == 0 && rs.bad) sFlag[2] = 1;
     const int n_rows = rs.cnt + rs.nw;
     // this query's tiles, ceil(tiles / splits) per split: the last split, which
@@ -346,40 +330,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const int r_end = min(n_rows, t_end * kRows);
     const int n_tiles = t_end - t_begin;
 
-    // ---- Q: the raw bf16 block [H][512] lands in the V tile, then bf16 -> f16 into
-    // the K-major 128-byte-swizzled sQ (heads >= H are zero); the worker threads
-    // start gathering the first tile's rows meanwhile (below)
-    const int wt = tid - 32;                          // worker index 0..255
+    // ---- a worker thread's places: softmax row (= TMEM lane) and heads; gather rows
     const uint32_t quarter = (uint32_t)(warp & 3);    // TMEM lanes 32 quarter ..
     const int row = (int)(quarter * 32 + lane);       // tile row == TMEM lane of this thread
-    const int half = (warp - 1) >> 2;                 // heads 32 half .. of its softmax
+    const int h0 = 16 * (warp >> 2);                  // heads h0 .. h0 + 15 of its softmax
 
-    // ---- gather.  Worker warp wg fills tile rows 16 wg .. 16 wg + 15.  A warp load
-    // covers 4 rows with 8 lanes each: lane l takes row 4x + (l >> 3) of the warp's
-    // 16 and, in channel chunk h (channels 256h ..), the 32 channels 256h + 32 sub ..
-    // (sub = l & 7): 16 contiguous code bytes and 2 scale bytes, so that each row's
-    // 8 lanes read one 128-byte line.  Register slot t = 4h + x.
-    const int wg = warp - 1;
+    // ---- gather.  Warp w fills tile rows 8w .. 8w + 7.  A warp load covers 4
+    // rows with 8 lanes each: lane l takes row 8w + 4x + (l >> 3) and, in channel
+    // chunk h (channels 256h ..), the 32 channels 256h + 32 sub .. (sub = l & 7):
+    // 16 contiguous code bytes and 2 scale bytes, so that each row's 8 lanes read
+    // one 128-byte line.  Register slot t = 2h + x.
     const int sub = lane & 7;
     const int rho = sub >> 1;                          // store rotation (bank groups)
-    uint4 gc[8];                  // codes of slot t
-    uint32_t gsc[8];              // the two scale bytes of those channels
-    uint32_t gkind = 0;           // bit t: FP4 row with data; bit 8 + t: window row
-    int gj = -1;                  // lanes 0-15: entry of row 16 wg + lane of the tile loaded next
+    uint4 gc[4];                  // codes of slot t
+    uint32_t gsc[4];              // the two scale bytes of those channels
+    uint32_t gkind = 0;           // bit t: FP4 row with data; bit 4 + t: window row
+    int gj = -1;                  // lanes 0-7: entry of row 8 warp + lane of the tile loaded next
     auto tile_row = [&](int tile, int r) { return r_begin + tile * kRows + r; };
     // entry of tile row r (-1 for window rows and rows past the end)
     auto entry = [&](int tile, int r) {
         const int g = tile_row(tile, r);
         return (g < r_end && g < rs.cnt) ? __ldg(p.idx + (int64_t)q * p.ld_idx + g) : -1;
     };
-    // the register slots of channel chunk hc (slots 4 hc .. 4 hc + 3) with tile `tile`
-    auto load_half = [&](int tile, int hc) {
+    // the register slots of channel chunk h (slots 2h, 2h + 1) with tile `tile`
+    auto load_half = [&](int tile, int h) {
 #pragma unroll
-        for (int t = 4 * hc; t < 4 * hc + 4; ++t) {
-            const int h = t >> 2, x = t & 3;
-            gkind &= ~((1u << t) | (1u << (8 + t)));
+        for (int x = 0; x < 2; ++x) {
+            const int t = 2 * h + x;
+            gkind &= ~((1u << t) | (1u << (4 + t)));
             const int rw = 4 * x + (lane >> 3);
-            const int g = tile_row(tile, 16 * wg + rw);
+            const int g = tile_row(tile, 8 * warp + rw);
             const int j = __shfl_sync(0xffffffffu, gj, rw);
             if (g < r_end && g < rs.cnt) {
                 if (j >= 0 && j < rs.nt) {
@@ -391,7 +371,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                     sFlag[2] = 1;
                 }
             } else if (g < r_end) {
-                gkind |= 1u << (8 + t);
+                gkind |= 1u << (4 + t);
             }
         }
     };
@@ -402,9 +382,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     // 16-byte bank groups (the source words are rotated to match).
     auto store_chunk = [&](int tile, int h) {
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int t = 4 * h + x;
-            const int r = 16 * wg + 4 * x + (lane >> 3);
+        for (int x = 0; x < 2; ++x) {
+            const int t = 2 * h + x;
+            const int r = 8 * warp + 4 * x + (lane >> 3);
             uint4 v[4];
             if (gkind & (1u << t)) {
                 const uint32_t p0 = scale_pair(gsc[t] & 0xFFu), p1 = scale_pair((gsc[t] >> 8) & 0xFFu);
@@ -423,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 }
 #pragma unroll
                 for (int m = 0; m < 4; ++m) v[m] = fp4x8_to_f16(w[m], sp[m]);
-            } else if (gkind & (1u << (8 + t))) {
+            } else if (gkind & (1u << (4 + t))) {
                 const int64_t pos = rs.lo + (tile_row(tile, r) - rs.cnt);
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     p.win + ((int64_t)rs.b * p.wcap + pos % p.wcap) * CSA2_D) + 32 * h + 4 * sub;
@@ -445,12 +425,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         }
     };
     // The rows of the tile after the next one are asked of L2 one tile before
-    // their loads (lanes 0-15: row 16 wg + lane, entry j; gj2 holds the entries
+    // their loads (lanes 0-7: row 8 warp + lane, entry j; gj2 holds the entries
     // of that tile)
     int gj2 = -1;
     auto prefetch_rows = [&](int tile, int j) {
-        const int g = tile_row(tile, 16 * wg + (lane & 15));
-        if (lane < 16 && g < r_end && g < rs.cnt && j >= 0 && j < rs.nt) {
+        const int g = tile_row(tile, 8 * warp + (lane & 7));
+        if (lane < 8 && g < r_end && g < rs.cnt && j >= 0 && j < rs.nt) {
             const int64_t r = rs.base + j;
             const uint8_t *c = p.codes + r * CSA2_CODE_BYTES;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(c));
@@ -458,15 +438,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p.scales + r * CSA2_SCALE_BYTES));
         }
     };
+    auto rows_entry = [&](int tile) { return lane < 8 ? entry(tile, 8 * warp + (lane & 7)) : -1; };
     int my_j = -1;                // entry of this thread's softmax row in the current tile
-    if (warp > 0 && n_tiles > 0) {
-        gj = lane < 16 ? entry(0, 16 * wg + (lane & 15)) : -1;
+    if (warp < kWorkerWarps && n_tiles > 0) {
+        gj = rows_entry(0);
         my_j = entry(0, row);
         load_half(0, 0);
         load_half(0, 1);
-        if (n_tiles > 1) gj = lane < 16 ? entry(1, 16 * wg + (lane & 15)) : -1;
-        if (n_tiles > 2) gj2 = lane < 16 ? entry(2, 16 * wg + (lane & 15)) : -1;
+        if (n_tiles > 1) gj = rows_entry(1);
+        if (n_tiles > 2) gj2 = rows_entry(2);
     }
+    // ---- Q: the raw bf16 block [H][512] lands in the V tile, then bf16 -> f16 into
+    // the K-major 128-byte-swizzled sQ (heads >= H are zero) while the first
+    // tile's rows are in flight
     {
         volatile int no_abort = 0;
         if (!mbar_wait(bar_q, 0, &no_abort)) sFlag[0] = 1;
@@ -489,8 +473,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     const uint32_t tS = tmem;                  // S^T: columns 0..63
     const uint32_t tO = tmem + 64;             // O^T block mb: columns 64 + 64 mb
     const uint32_t tLsum = tmem + 320;         // running sums: columns 320 .. 383
+    const uint32_t lane_q = (quarter * 32u) << 16;
 
-    if (warp == 0) {
+    const uint32_t tL = tLsum + (uint32_t)h0 + lane_q;   // (workers) running sums, see below
+    if (warp == kWorkerWarps) {
         // ============================================== MMA issuer
         if (lane == 0 && n_tiles > 0) {
             const uint32_t id_qk = instr_desc(128, kHeads, 0, 0, 0, 0);
@@ -530,63 +516,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                     if (mb & 1) mma_commit(&bar_o[mb >> 1]);
                 }
             }
-            if (*abort_flag) count_event(p.counters, CSA2_CNT_TIMEOUT);
-            // every MMA of this thread has completed before TMEM is released
-            volatile int no_abort = 0;
+            // completes once every MMA issued above has completed
             mma_commit(bar_done);
-            mbar_wait(bar_done, 0, &no_abort);
         }
     } else {
-        // ============================================== 8 worker warps
+        // ============================================== 16 worker warps
         const float l2s = p.sm_scale * 1.4426950408889634f;
-        const int h0 = 32 * half;                      // this thread's heads h0 .. h0+31
-        // this thread's share of the running sums, its rows' P for heads h0 .. h0+31,
+        // this thread's share of the running sums, its row's P for heads h0 .. h0+15,
         // accumulates in TMEM columns 320 + h0 .. (its lane = its row): rescaled with
         // the reference max, reduced over the rows once, at the end
-        const uint32_t tL = tLsum + (uint32_t)h0 + ((quarter * 32u) << 16);
         {
-            float z[32];
+            float z[16];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) z[h] = 0.f;
-            tmem_st32(tL, z);
+            for (int h = 0; h < 16; ++h) z[h] = 0.f;
+            tmem_st16(tL, z);
             tmem_wait_st();
         }
-        bool ok = true;
+        bool ok = !sFlag[0];
         for (int i = 0; i < n_tiles && ok; ++i) {
             if (i + 2 < n_tiles) prefetch_rows(i + 2, gj2);
             const int g_row = tile_row(i, row);
             const bool valid = g_row < r_end && (g_row >= rs.cnt || (my_j >= 0 && my_j < rs.nt));
             // chunk h of this tile goes where the previous tile's PV product has
-            // released it (its channel blocks 2h, 2h + 1 done)
+            // released it (its channel blocks 2h, 2h + 1 done); a warp that gives
+            // up on a wait still arrives, and the vote below stops every worker
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                bool got = true;
                 if (i > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait<true>(&bar_o[h], (i - 1) & 1, abort_flag));
-                    if (!ok) break;
+                    got = __all_sync(0xffffffffu, mbar_wait<true>(&bar_o[h], (i - 1) & 1, abort_flag));
                     tc_fence_after();
                 }
-                store_chunk(i, h);
+                if (got) store_chunk(i, h);
+                else ok = false;
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_v[h]);
             }
-            if (!ok) break;
             // the next tile's codes: chunk 0 while the QK product finishes, chunk 1
             // (below) while the PV product of this tile starts
             const bool more = i + 1 < n_tiles;
             int my_j_next = -1;
             if (more) load_half(i + 1, 0);
 
-            // ---- softmax of this row, heads h0 .. h0+31
-            ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_s, i & 1, abort_flag));
-            if (!ok) break;
+            // ---- softmax of this row, heads h0 .. h0+15
+            const bool got_s = ok && mbar_wait<true>(bar_s, i & 1, abort_flag);
             tc_fence_after();
-            float x[32];
-            tmem_ld32(tS + ((quarter * 32u) << 16) + (uint32_t)h0, x);
-            tmem_wait_ld();
+            float x[16];
+            if (got_s) {
+                tmem_ld16(tS + lane_q + (uint32_t)h0, x);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int h = 0; h < 16; ++h) x[h] = 0.f;
+            }
             bool over = false;
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
+            for (int h4 = 0; h4 < 4; ++h4) {
                 const float4 m4 = reinterpret_cast<const float4 *>(sM + h0)[h4];
                 const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
@@ -599,64 +585,66 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             // the reference max moves only when some logit is more than 8 above it;
             // the flag holds the number of the last tile that needed it (no reset)
             if (over) sFlag[3] = i + 1;
-            named_sync_all_workers();
-            const bool need_max = sFlag[3] == i + 1;
-            if (need_max) {
-                float r[32];
+            ok = workers_and(got_s);
+            if (!ok) {
+                if (tid == 0) *abort_flag = 1;     // (the issuer stops waiting)
+                break;
+            }
+            if (sFlag[3] == i + 1) {
+                float r[16];
 #pragma unroll
-                for (int h = 0; h < 32; ++h) r[h] = x[h];
-                warp_reduce32<true>(r, lane);
-                sRed[quarter * 64 + h0 + lane] = r[0];
-                named_sync_all_workers();
-                if (wt < 64) {
-                    const float tmax = fmaxf(fmaxf(sRed[wt], sRed[64 + wt]),
-                                             fmaxf(sRed[128 + wt], sRed[192 + wt]));
-                    const float m_old = sM[wt];
+                for (int h = 0; h < 16; ++h) r[h] = x[h];
+                warp_reduce16<true>(r, lane);
+                if (lane < 16) sRed[quarter * 64 + h0 + lane] = r[0];
+                workers_sync();
+                if (tid < 64) {
+                    const float tmax = fmaxf(fmaxf(sRed[tid], sRed[64 + tid]),
+                                             fmaxf(sRed[128 + tid], sRed[192 + tid]));
+                    const float m_old = sM[tid];
                     float alpha = 1.f;
                     if (tmax > m_old + kRescaleThreshold) {
                         alpha = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - tmax);
-                        sM[wt] = tmax;
+                        sM[tid] = tmax;
                         if (i > 0) sFlag[1] = 1;
                     }
-                    sAlpha[wt] = alpha;
+                    sAlpha[tid] = alpha;
                 }
-                named_sync_all_workers();
-                const bool rescale = sFlag[1] != 0;
-                if (rescale) {
+                workers_sync();
+                if (sFlag[1] != 0) {
                     // O^T and the running sums *= alpha per head; PV of the previous
                     // tile has completed (both of its chunk barriers were waited above)
-                    float al[32];
+                    float al[16];
 #pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4) {
+                    for (int h4 = 0; h4 < 4; ++h4) {
                         const float4 a4 = reinterpret_cast<const float4 *>(sAlpha + h0)[h4];
                         al[4 * h4] = a4.x; al[4 * h4 + 1] = a4.y; al[4 * h4 + 2] = a4.z; al[4 * h4 + 3] = a4.w;
                     }
                     {
-                        float o[32];
-                        tmem_ld32(tL, o);
+                        float o[16];
+                        tmem_ld16(tL, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < 32; ++h) o[h] *= al[h];
-                        tmem_st32(tL, o);
+                        for (int h = 0; h < 16; ++h) o[h] *= al[h];
+                        tmem_st16(tL, o);
                     }
 #pragma unroll 1
                     for (int mb = 0; mb < 4; ++mb) {
-                        float o[32];
-                        const uint32_t ta = tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16);
-                        tmem_ld32(ta, o);
+                        float o[16];
+                        const uint32_t ta = tO + 64 * mb + (uint32_t)h0 + lane_q;
+                        tmem_ld16(ta, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < 32; ++h) o[h] *= al[h];
-                        tmem_st32(ta, o);
+                        for (int h = 0; h < 16; ++h) o[h] *= al[h];
+                        tmem_st16(ta, o);
                     }
                     tmem_wait_st();
                 }
-                named_sync_all_workers();
-                if (wt == 0) sFlag[1] = 0;
+                workers_sync();
+                if (tid == 0) sFlag[1] = 0;
             }
-            // P = 2^(x - m) as f16 into sP; the row sums stay in registers
+            // P = 2^(x - m) as f16 into sP (pieces h0 / 8, h0 / 8 + 1 of its row)
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
+            for (int h4 = 0; h4 < 4; ++h4) {
                 const float4 m4 = reinterpret_cast<const float4 *>(sM + h0)[h4];
                 const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
@@ -666,12 +654,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 }
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 const uint4 v = make_uint4(f32x2_to_f16x2(x[8 * c], x[8 * c + 1]),
                                            f32x2_to_f16x2(x[8 * c + 2], x[8 * c + 3]),
                                            f32x2_to_f16x2(x[8 * c + 4], x[8 * c + 5]),
                                            f32x2_to_f16x2(x[8 * c + 6], x[8 * c + 7]));
-                *reinterpret_cast<uint4 *>(sP + sw128(row, 4 * half + c)) = v;
+                *reinterpret_cast<uint4 *>(sP + sw128(row, h0 / 8 + c)) = v;
             }
             fence_async_smem();
             tc_fence_before();
@@ -680,38 +668,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             if (more) {
                 load_half(i + 1, 1);
                 gj = gj2;
-                if (i + 3 < n_tiles) gj2 = lane < 16 ? entry(i + 3, 16 * wg + (lane & 15)) : -1;
+                if (i + 3 < n_tiles) gj2 = rows_entry(i + 3);
                 my_j_next = entry(i + 1, row);
             }
             {
-                float o[32];
-                tmem_ld32(tL, o);
+                float o[16];
+                tmem_ld16(tL, o);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 32; ++h) o[h] += x[h];
-                tmem_st32(tL, o);
+                for (int h = 0; h < 16; ++h) o[h] += x[h];
+                tmem_st16(tL, o);
                 tmem_wait_st();
             }
             my_j = my_j_next;
         }
         if (!ok) *abort_flag = 1;
-        // the running sums: over the warp's 32 rows, then the 4 quarters
-        float lsum[32];
-        tmem_ld32(tL, lsum);
-        tmem_wait_ld();
-        warp_reduce32<false>(lsum, lane);
-        sRedL[quarter * 64 + h0 + lane] = lsum[0];
-        named_sync_all_workers();
-        if (wt < 64) sL[wt] = (sRedL[wt] + sRedL[64 + wt]) + (sRedL[128 + wt] + sRedL[192 + wt]);
-
-        // ---- epilogue: O^T (unnormalised) of this split
-        if (ok && n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[1], (n_tiles - 1) & 1, abort_flag));
-            tc_fence_after();
-        }
-        if (!ok) *abort_flag = 1;
-        if (wt == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
     }
+    // every MMA issued has completed before O^T is read and TMEM released
+    if (n_tiles > 0) {
+        volatile int no_abort = 0;
+        if (!mbar_wait<true>(bar_done, 0, &no_abort)) *abort_flag = 1;
+        tc_fence_after();
+    }
+    // the running sums: over the warp's 32 rows, then the 4 quarters
+    if (warp < kWorkerWarps) {
+        float lsum[16];
+        tmem_ld16(tL, lsum);
+        tmem_wait_ld();
+        warp_reduce16<false>(lsum, lane);
+        if (lane < 16) sRedL[quarter * 64 + h0 + lane] = lsum[0];
+    }
+    __syncthreads();
+    if (tid < 64) sL[tid] = (sRedL[tid] + sRedL[64 + tid]) + (sRedL[128 + tid] + sRedL[192 + tid]);
+    if (tid == 0 && sFlag[2]) count_event(p.counters, CSA2_CNT_BAD_INPUT);
+    if (tid == 0 && *abort_flag) count_event(p.counters, CSA2_CNT_TIMEOUT);
 
     {
         // ---- merge of the cluster's splits.  Every thread of every CTA reaches
@@ -721,9 +711,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         float *sFac = reinterpret_cast<float *>(sP);          // [split][head]
         float *sX = reinterpret_cast<float *>(sV);            // receive area (V and Q tiles)
         cluster_wait();              // (arrived at the start) every CTA of the cluster runs
-        // the workers' sM and sL are final before the MMA warp (threads 0 .. 31)
-        // reads them: it takes no part in the workers' named barriers
-        __syncthreads();
         // this split's reference max and sum go to every CTA's own table (a peer's
         // V, Q and P tiles may still be in use)
         if (tid < 64) {
@@ -752,38 +739,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                 p.lse[(int64_t)q * H + tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
         }
         __syncthreads();
-        if (warp > 0) {
-            const int h0 = 32 * half;
+        if (warp < kWorkerWarps) {
             const bool any = !*abort_flag && n_tiles > 0;
-            float f[32];
+            float f[16];
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
+            for (int h4 = 0; h4 < 4; ++h4) {
                 const float4 a4 = reinterpret_cast<const float4 *>(sFac + rank * 64 + h0)[h4];
                 f[4 * h4] = a4.x; f[4 * h4 + 1] = a4.y; f[4 * h4 + 2] = a4.z; f[4 * h4 + 3] = a4.w;
             }
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
-                float o[32];
+                float o[16];
                 if (any) {
-                    tmem_ld32(tO + 64 * mb + (uint32_t)h0 + ((quarter * 32u) << 16), o);
+                    tmem_ld16(tO + 64 * mb + (uint32_t)h0 + lane_q, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) o[h] = 0.f;
+                    for (int h = 0; h < 16; ++h) o[h] = 0.f;
                 }
                 const int c = 4 * mb + (int)quarter;
                 if (S == 1) {
                     // a single split: its scaled O^T is the output (lane = channel)
                     float *od = p.out + ((int64_t)q * H + h0) * CSA2_D + 32 * c + lane;
 #pragma unroll
-                    for (int h = 0; h < 32; ++h)
+                    for (int h = 0; h < 16; ++h)
                         if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
                     continue;
                 }
                 float *dst = cluster.map_shared_rank(sX, c % S) +
                              ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) dst[h * 32] = o[h] * f[h];
+                for (int h = 0; h < 16; ++h) dst[h * 32] = o[h] * f[h];
             }
         }
         if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
