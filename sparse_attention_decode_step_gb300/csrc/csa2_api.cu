@@ -203,13 +203,12 @@ csa2_status csa2_quantize_append_project(const csa2_cache *cache, const float *C
 
 namespace {
 
-// The entry points' bodies; hist0 (nullable, [nq][2048]) is counted by the
-// decode indexer for the top-k that follows inside csa2_layer_step.
+// The entry points' bodies (shared with csa2_layer_step).
 csa2_status index_full_impl(const csa2_cache *cache, const csa2_queries *queries,
                             const float *q_idx, const float *w, int32_t h_idx, int64_t max_n,
                             float *scores, int64_t ld_scores, float *blockmax,
                             int64_t ld_blockmax, int32_t *n_valid, void *workspace,
-                            size_t ws_bytes, uint32_t *counters, uint32_t *hist0, void *stream)
+                            size_t ws_bytes, uint32_t *counters, void *stream)
 {
     csa2_status s = check_index_args(cache, queries, q_idx, w, h_idx, scores, ld_scores, workspace);
     if (s != CSA2_OK) return s;
@@ -225,7 +224,7 @@ csa2_status index_full_impl(const csa2_cache *cache, const csa2_queries *queries
                  CSA2_ERR_CAPACITY);
     return cuda_status(launch_index(*cache, *queries, q_idx, w, h_idx, max_n, nullptr, nullptr, 0,
                                     scores, ld_scores, blockmax, ld_blockmax, n_valid, workspace,
-                                    counters, hist0, static_cast<cudaStream_t>(stream)));
+                                    counters, static_cast<cudaStream_t>(stream)));
 }
 
 csa2_status index_reindex_impl(const csa2_cache *cache, const csa2_queries *queries,
@@ -233,7 +232,7 @@ csa2_status index_reindex_impl(const csa2_cache *cache, const csa2_queries *quer
                                const int32_t *pool_blk, const int32_t *pool_n,
                                int32_t pool_blocks, float *scores, int64_t ld_scores,
                                int32_t *n_valid, void *workspace, size_t ws_bytes,
-                               uint32_t *counters, uint32_t *hist0, void *stream)
+                               uint32_t *counters, void *stream)
 {
     csa2_status s = check_index_args(cache, queries, q_idx, w, h_idx, scores, ld_scores, workspace);
     if (s != CSA2_OK) return s;
@@ -247,13 +246,13 @@ csa2_status index_reindex_impl(const csa2_cache *cache, const csa2_queries *quer
                  CSA2_ERR_CAPACITY);
     return cuda_status(launch_index(*cache, *queries, q_idx, w, h_idx, 8LL * pool_blocks, pool_blk,
                                     pool_n, pool_blocks, scores, ld_scores, nullptr, 0, n_valid,
-                                    workspace, counters, hist0, static_cast<cudaStream_t>(stream)));
+                                    workspace, counters, static_cast<cudaStream_t>(stream)));
 }
 
 csa2_status topk_impl(const float *scores, int64_t ld_scores, const int32_t *n_valid,
                       const int32_t *pool_blk, int32_t pool_blocks, int32_t nq, int64_t max_n,
                       int32_t k, int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out,
-                      void *workspace, size_t ws_bytes, const uint32_t *hist0, void *stream)
+                      void *workspace, size_t ws_bytes, void *stream)
 {
     CSA2_REQUIRE(nq >= 0, CSA2_ERR_INVALID_ARG);
     if (nq == 0) return CSA2_OK;
@@ -270,7 +269,7 @@ csa2_status topk_impl(const float *scores, int64_t ld_scores, const int32_t *n_v
     CSA2_REQUIRE(max_n < (1LL << 31), CSA2_ERR_INVALID_ARG);
     CSA2_REQUIRE(ws_bytes >= topk_workspace_bytes(nq, max_n), CSA2_ERR_CAPACITY);
     return cuda_status(launch_topk(scores, ld_scores, n_valid, 0, pool_blk, pool_blocks, nq, max_n,
-                                   k, idx_out, ld_idx, cnt_out, workspace, hist0,
+                                   k, idx_out, ld_idx, cnt_out, workspace,
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -285,7 +284,7 @@ csa2_status csa2_index_full(const csa2_cache *cache, const csa2_queries *queries
                             size_t ws_bytes, uint32_t *counters, void *stream)
 {
     return index_full_impl(cache, queries, q_idx, w, h_idx, max_n, scores, ld_scores, blockmax,
-                           ld_blockmax, n_valid, workspace, ws_bytes, counters, nullptr, stream);
+                           ld_blockmax, n_valid, workspace, ws_bytes, counters, stream);
 }
 
 csa2_status csa2_index_reindex(const csa2_cache *cache, const csa2_queries *queries,
@@ -296,8 +295,7 @@ csa2_status csa2_index_reindex(const csa2_cache *cache, const csa2_queries *quer
                                uint32_t *counters, void *stream)
 {
     return index_reindex_impl(cache, queries, q_idx, w, h_idx, pool_blk, pool_n, pool_blocks,
-                              scores, ld_scores, n_valid, workspace, ws_bytes, counters, nullptr,
-                              stream);
+                              scores, ld_scores, n_valid, workspace, ws_bytes, counters, stream);
 }
 
 csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_valid,
@@ -306,7 +304,7 @@ csa2_status csa2_topk(const float *scores, int64_t ld_scores, const int32_t *n_v
                       void *workspace, size_t ws_bytes, void *stream)
 {
     return topk_impl(scores, ld_scores, n_valid, pool_blk, pool_blocks, nq, max_n, k, idx_out,
-                     ld_idx, cnt_out, workspace, ws_bytes, nullptr, stream);
+                     ld_idx, cnt_out, workspace, ws_bytes, stream);
 }
 
 csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const int32_t *n_valid,
@@ -407,8 +405,7 @@ namespace {
 struct LayerPlan {
     int64_t max_n, ld, ld_bm;
     int chunk;                    // queries per indexer/top-k chunk
-    bool hist;                    // the indexer counts the top-k's first histogram
-    size_t off_scores, off_bm, off_nv, off_hist, off_idx_ws, off_topk_ws, off_attn_ws, total;
+    size_t off_scores, off_bm, off_nv, off_idx_ws, off_topk_ws, off_attn_ws, total;
 };
 
 bool plan_layer(const csa2_layer_args *a, LayerPlan *pl)
@@ -435,11 +432,6 @@ bool plan_layer(const csa2_layer_args *a, LayerPlan *pl)
         if (a->mode == CSA2_FULL && a->build_pool) o += align_up((size_t)chunk * pl->ld_bm * 4, 256);
         pl->off_nv = o;
         o += align_up((size_t)nq * 4, 256);
-        // decode layers (one query per sequence, a Reindex pool or a Full context
-        // up to 256K entries): the indexer counts the top-k's first digit
-        pl->hist = (a->mode == CSA2_REINDEX || group == 1) && topk_select_fits(pl->max_n, a->k);
-        pl->off_hist = o;
-        if (pl->hist) o += align_up((size_t)chunk * 2048 * 4, 256);
         pl->off_idx_ws = o;
         o += align_up(index_workspace_bytes((int)chunk, a->mode == CSA2_FULL ? group : 1, a->h_idx,
                                             a->cache->d_idx),
@@ -494,7 +486,6 @@ csa2_status csa2_layer_step(const csa2_layer_args *a, void *stream)
         float *scores = reinterpret_cast<float *>(ws + pl.off_scores);
         float *bm = reinterpret_cast<float *>(ws + pl.off_bm);
         int32_t *nv = reinterpret_cast<int32_t *>(ws + pl.off_nv);
-        uint32_t *hist = pl.hist ? reinterpret_cast<uint32_t *>(ws + pl.off_hist) : nullptr;
         void *iws = ws + pl.off_idx_ws;
         void *tws = ws + pl.off_topk_ws;
         const size_t iws_bytes = pl.off_topk_ws - pl.off_idx_ws;
@@ -512,16 +503,16 @@ csa2_status csa2_layer_step(const csa2_layer_args *a, void *stream)
             if (a->mode == CSA2_FULL) {
                 s = index_full_impl(a->cache, &sub, qi, wi, a->h_idx, pl.max_n, scores, pl.ld,
                                     a->build_pool ? bm : nullptr, pl.ld_bm, nv + q0, iws,
-                                    iws_bytes, a->counters, hist, stream);
+                                    iws_bytes, a->counters, stream);
             } else {
                 s = index_reindex_impl(a->cache, &sub, qi, wi, a->h_idx, pblk, pn, a->pool_blocks,
-                                       scores, pl.ld, nv + q0, iws, iws_bytes, a->counters, hist,
+                                       scores, pl.ld, nv + q0, iws, iws_bytes, a->counters,
                                        stream);
             }
             if (s != CSA2_OK) return s;
             s = topk_impl(scores, pl.ld, nv + q0, a->mode == CSA2_REINDEX ? pblk : nullptr,
                           a->pool_blocks, nc, pl.max_n, a->k, a->idx + (int64_t)q0 * a->k, a->k,
-                          a->cnt + q0, tws, tws_bytes, hist, stream);
+                          a->cnt + q0, tws, tws_bytes, stream);
             if (s != CSA2_OK) return s;
             if (a->mode == CSA2_FULL && a->build_pool) {
                 s = csa2_pool_select(bm, pl.ld_bm, nv + q0, nc, pl.max_n, a->pool_blocks, pblk, pn,

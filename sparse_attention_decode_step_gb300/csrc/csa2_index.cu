@@ -38,7 +38,6 @@ constexpr int kIdxThreadsMax = kIdxThreadsGrouped;
 constexpr int kTile = 128;
 constexpr int kEpiBatch = 4;          // tiles the epilogue takes per pass (decode)
 constexpr int kMaxGroupCols = 256;     // group * h_idx (the MMA's N) is at most 256
-constexpr int kHistBins = 2048;        // histogram of the top 11 bits of the score keys (decode)
 // the epilogue warps (2 ..) only
 template <int kEpiThreads>
 __device__ __forceinline__ void named_sync_epilogue()
@@ -71,9 +70,6 @@ struct IndexParams {
     int64_t ld_bm;
     int32_t *n_valid;
     uint32_t *counters;
-    // decode (group 1) only, nullable: per-query histogram of the top 11 bits of
-    // the score keys, the first radix digit of the top-k that follows [nq][2048]
-    uint32_t *hist0;
 };
 
 // Byte offset of (row r, byte c) in a K-major tile with `rowb`-byte rows under
@@ -128,9 +124,6 @@ __global__ void __launch_bounds__(256) index_prep_kernel(IndexParams p)
         if (s_bad) count_event(p.counters, CSA2_CNT_BAD_INPUT);
         p.gtiles[g] = s_bad ? 0 : (s_maxn + kTile - 1) / kTile;
     }
-    if (p.hist0 != nullptr)
-        for (int i = threadIdx.x; i < p.group * kHistBins; i += blockDim.x)
-            p.hist0[(int64_t)q0 * kHistBins + i] = 0u;
     // FP8 query rows: row r = (query in group) * h_idx + head; padding rows = 0
     uint8_t *img = p.q8img + (int64_t)g * p.n_pad * p.d_idx;
     for (int r = warp; r < p.n_pad; r += blockDim.x / 32) {
@@ -264,7 +257,6 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
     float *sWg = reinterpret_cast<float *>(                              // [group * h_idx] (group > 1)
         (reinterpret_cast<uintptr_t>(s_scan + kIdxThreadsMax) + 15) & ~(uintptr_t)15);
     int32_t *sNg = reinterpret_cast<int32_t *>(sWg + kMaxGroupCols); // [group]
-    uint32_t *sHist = reinterpret_cast<uint32_t *>(sNg + kMaxGroupCols); // [4 warps][kHistBins] (hist0)
 
     volatile int *abort_flag = sI;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -533,32 +525,11 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
         int prev_g = -1;
         float wsr[16];
         int ntq = 0;
-        // the top-k's first histogram: each epilogue warp counts into its own
-        // shared-memory copy (one atomic per lane, no contention between warps and
-        // no barrier between them) and adds it to the query's global row when the
-        // query changes
-        const bool do_hist = !kTwoPerSm && p.hist0 != nullptr && p.group == 1;
-        uint32_t *wh = sHist + (warp - 2) * kHistBins;
-        auto flush_hist = [&](int qh) {
-            for (int b = lane; b < kHistBins; b += 32) {
-                const uint32_t v = wh[b];
-                if (v) {
-                    atomicAdd(p.hist0 + (int64_t)qh * kHistBins + b, v);
-                    wh[b] = 0u;
-                }
-            }
-            __syncwarp();
-        };
-        if (do_hist) {
-            for (int b = lane; b < kHistBins; b += 32) wh[b] = 0u;
-            __syncwarp();
-        }
         while (it.u < it.u1) {
             const int g = it.g, t = it.t;
             const int q0 = g * p.group;
             // (kTwoPerSm is only launched for groups of more than 64 / h_idx queries)
             if (!kTwoPerSm && g != prev_g && p.group == 1) {
-                if (do_hist && prev_g >= 0) flush_hist(prev_g);
                 for (int h = 0; h < 16; ++h) wsr[h] = (h < p.h_idx) ? p.ws[(int64_t)q0 * p.h_idx + h] : 0.f;
                 ntq = p.nt[q0];
                 prev_g = g;
@@ -615,7 +586,6 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
                         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                         if ((lane & 7) == 0 && valid) p.blockmax[(int64_t)q0 * p.ld_bm + (j >> 3)] = bm;
                     }
-                    if (do_hist && valid) atomicAdd(wh + (score_key(sc) >> 21), 1u);
                 }
                 // this warp is done with the stages' key scales: its share of their release
                 __syncwarp();
@@ -716,7 +686,6 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
             unit_next(it, p.gtiles, p.n_groups);
         }
         if (it.u < it.u1) *abort_flag = 1;
-        if (do_hist && prev_g >= 0) flush_hist(prev_g);
     }
 
     tc_fence_before();
@@ -728,14 +697,14 @@ __global__ void __launch_bounds__(kTwoPerSm ? kIdxThreadsGrouped : kIdxThreads, 
 }
 
 // ---------------------------------------------------------------- host side
-static size_t index_smem_bytes(int d_idx, int n_pad, int stages, int nacc, bool hist)
+static size_t index_smem_bytes(int d_idx, int n_pad, int stages, int nacc)
 {
     const size_t a = (size_t)stages * kTile * d_idx;
     const size_t k = (size_t)stages * kTile * 4;
     const size_t b = 2 * (((size_t)n_pad * d_idx + 1023) & ~(size_t)1023);
     const size_t bars = (size_t)(2 * stages + 4 + 2 * (nacc > 2 ? nacc : 2) + 1) * 8;
     return 1024 /*align*/ + a + k + 1024 /*align B*/ + b + bars + 64 + kIdxThreadsMax * 8 + 16 +
-           kMaxGroupCols * 4 + kMaxGroupCols * 4 + (hist ? 4 * kHistBins * 4 : 0);
+           kMaxGroupCols * 4 + kMaxGroupCols * 4;
 }
 
 size_t index_workspace_bytes(int nq, int group, int h_idx, int d_idx)
@@ -753,10 +722,9 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
                          const float *w, int h_idx, int64_t max_n, const int32_t *pool_blk,
                          const int32_t *pool_n, int pool_blocks, float *scores, int64_t ld,
                          float *blockmax, int64_t ld_bm, int32_t *n_valid, void *ws,
-                         uint32_t *counters, uint32_t *hist0, cudaStream_t st)
+                         uint32_t *counters, cudaStream_t st)
 {
     IndexParams p{};
-    p.hist0 = qs.group == 1 ? hist0 : nullptr;
     p.kscale = c.kscale;
     p.seq_base = c.seq_base;
     p.seq_len = c.seq_len;
@@ -804,11 +772,9 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
     // query groups (N up to 256): two CTAs per SM, each with a shallow pipeline
     // and one accumulator, whose MMAs and epilogues interleave
     const bool grouped = p.n_pad > 64;
-    const bool hist = !grouped && p.hist0 != nullptr;
-    // (the four per-warp histograms take one key stage's room at d_idx 128)
-    const int stages = grouped ? 2 : (c.d_idx == 128 ? (hist ? 11 : 12) : 16);
+    const int stages = grouped ? 2 : (c.d_idx == 128 ? 12 : 16);
     const int nacc = grouped ? 1 : 8;
-    const size_t smem = index_smem_bytes(c.d_idx, p.n_pad, stages, nacc, hist);
+    const size_t smem = index_smem_bytes(c.d_idx, p.n_pad, stages, nacc);
     const int grid = device_sm_count() * (grouped ? 2 : 1);
     auto run = [&](auto k) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -65,18 +65,14 @@ cudaError_t launch_index(const csa2_cache &c, const csa2_queries &qs, const floa
                          const float *w, int h_idx, int64_t max_n, const int32_t *pool_blk,
                          const int32_t *pool_n, int pool_blocks, float *scores, int64_t ld,
                          float *blockmax, int64_t ld_bm, int32_t *n_valid, void *ws,
-                         uint32_t *counters, uint32_t *hist0, cudaStream_t st);
+                         uint32_t *counters, cudaStream_t st);
 
 // ---- top-k and pool
 size_t topk_workspace_bytes(int nq, int64_t max_n);
-// hist0 (nullable): [nq][2048] histogram of the top 11 bits of each query's
-// score keys, counted by the indexer that wrote the scores (decode layers).
 cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid, int n_div8,
                         const int32_t *pool_blk, int pool_blocks, int nq, int64_t max_n, int k,
                         int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out, void *ws,
-                        const uint32_t *hist0, cudaStream_t st);
-// Whether launch_topk takes its cluster selection when given hist0.
-bool topk_select_fits(int64_t max_n, int k);
+                        cudaStream_t st);
 cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_valid, int nq,
                         int64_t max_n, int pool_blocks, int32_t *pool_blk, int32_t *pool_n,
                         void *ws, cudaStream_t st);

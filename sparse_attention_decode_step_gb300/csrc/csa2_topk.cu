@@ -50,7 +50,6 @@ struct TopkParams {
     TopkState *state;           // [nq]
     uint32_t *ccount;           // [nq][n_chunks][2]  (gt, eq)
     uint32_t *coff;             // [nq][n_chunks][2]  (out offset, eq before)
-    const uint32_t *hist0;      // [nq][kBins] first-digit histogram from the indexer, or null
 };
 
 __device__ __forceinline__ int round_shift(int r) { return r == 0 ? 21 : (r == 1 ? 10 : 0); }
@@ -539,383 +538,6 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     }
 }
 
-// ---------------------------------------------------------------- decode: one cluster per query
-// For a decode layer whose indexer counted the histogram of the top 11 key bits
-// (hist0), with up to kSelMaxN candidates: one cluster of C CTAs (1024 threads
-// each) per query, every CTA a contiguous slice of the score row (read from
-// L2, where the indexer left it) and each of its warps a contiguous segment of
-// the slice, all of whose 16-byte loads are in flight together.  From hist0
-// every CTA knows the bin d0 (top 11 bits) that holds the k-th key, with fewer
-// than k keys above it.  One pass marks the keys above bin d0 in a bitmap of
-// the slice and lists the keys in bin d0 (the candidates), counted by their
-// next 11 bits; the cluster's summed counts give the 22-bit bin m1 of the
-// k-th key.  Candidates above m1 join the bitmap.  The few keys inside m1 are
-// copied to every CTA of the cluster, so that each finds the exact k-th key T
-// and its own place in the output by itself: keys above T are all taken, and
-// of the keys equal to T the lowest positions (slices in order).  Each CTA
-// writes the set bits of its bitmap, ascending, at its offset in the output.
-// When bin m1 is too full to copy (heavy ties), the last 10 bits are counted
-// over the cluster as well, which costs one more cluster barrier.  Order never
-// depends on the candidate list, so a slice whose candidates overflow the list
-// re-reads them from the score row.
-constexpr int kSelThreads = 1024;
-constexpr int kSelSlice = 16384;                       // positions per CTA, nominal
-constexpr int kSelMaxSlice = 32768;                    // bitmap words: 1024 (one per thread)
-constexpr int kSelMaxCtas = 8;
-constexpr int kSelCand = 4096;                         // candidates listed per CTA
-constexpr int kSelWarpCand = kSelCand / (kSelThreads / 32);   // 128 per warp
-constexpr int kSelCopy = 4096;                         // keys of bin m1 copied to a CTA, all slices
-constexpr int kSelLoads = 5;                           // 16-byte loads per lane and step
-constexpr int kSelStep = 128 * kSelLoads;              // positions per warp and step
-constexpr int64_t kSelMaxN = (int64_t)kSelMaxSlice * kSelMaxCtas;   // 262,144
-
-// Block-wide exclusive scan of one 32-bit value per thread (1024 threads).
-__device__ __forceinline__ uint32_t scan_sel(uint32_t v, uint32_t *s_warp, uint32_t *total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t w = s_warp[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        s_warp[lane] = w;                                  // inclusive warp totals
-    }
-    __syncthreads();
-    const uint32_t before = warp > 0 ? s_warp[warp - 1] : 0u;
-    if (total) *total = s_warp[31];
-    __syncthreads();
-    return before + x - v;
-}
-
-// Digit of a round: bins `nb` (descending from nb - 1), counts in h; the digit
-// d has count(> d) < need <= count(>= d).  Every thread returns d and count(> d).
-__device__ __forceinline__ void pick_digit(const uint32_t *h, int nb, uint32_t need,
-                                           uint32_t *s_warp, uint32_t *s_res, uint32_t &d,
-                                           uint32_t &above)
-{
-    const int per = (nb + kSelThreads - 1) / kSelThreads;    // 1 or 2
-    uint32_t c[2] = {0u, 0u}, mine = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int b = nb - 1 - (threadIdx.x * per + i);
-        if (i < per && b >= 0) c[i] = h[b];
-        mine += c[i];
-    }
-    if (threadIdx.x == 0) { s_res[0] = 0u; s_res[1] = 0u; }
-    const uint32_t before = scan_sel(mine, s_warp, nullptr);
-    if (before < need && need <= before + mine) {
-        uint32_t acc = before;
-        for (int i = 0; i < per; ++i) {
-            if (need <= acc + c[i]) {
-                s_res[0] = (uint32_t)(nb - 1 - (threadIdx.x * per + i));
-                s_res[1] = acc;
-                break;
-            }
-            acc += c[i];
-        }
-    }
-    __syncthreads();
-    d = s_res[0];
-    above = s_res[1];
-    __syncthreads();
-}
-
-struct SelShared {
-    uint32_t bits[kSelMaxSlice / 32];      // taken positions of the slice
-    uint32_t ties[kSelMaxSlice / 32];      // positions of the slice whose key equals T
-    uint32_t h1[2048];                     // bin-d0 keys of the slice by bits 10..20 (read by the cluster)
-    uint32_t h2[1024];                     // bin-m1 keys of the slice by bits 0..9 (read by the cluster)
-    uint32_t hs[2048];                     // counts summed over the cluster
-    uint32_t cand_key[kSelCand];
-    int32_t cand_pos[kSelCand];            // (positions relative to the slice)
-    uint32_t copy_key[kSelCopy];           // keys of bin m1: source slice r at [r * cap, ..)  (peers write)
-    uint32_t pub[3][kSelMaxCtas];          // per source slice (peers write): taken so far, keys in m1, ties
-    uint32_t stat[2][kSelMaxCtas];         // per source slice: copied keys above T, equal to T
-    uint32_t cnt[4];                       // list overflow, keys in m1, ties
-    uint32_t wcnt[kSelThreads / 32];       // candidates found by each warp
-    uint32_t s_warp[kSelThreads / 32];
-    uint32_t s_res[2];
-};
-
-__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkParams p, int slice)
-{
-    pdl_wait();
-    pdl_trigger();
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-    extern __shared__ __align__(16) uint8_t sel_smem[];
-    SelShared &sh = *reinterpret_cast<SelShared *>(sel_smem);
-    const int q = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    int n = p.n_valid[q];
-    if (p.n_div8) n = (n + 7) / 8;
-    if (n < 0) n = 0;
-    if (n > p.max_n) n = (int)p.max_n;
-    const float *row = p.scores + (int64_t)q * p.ld;
-    int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
-    const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
-    auto pos_of = [&](int i) { return pb ? 8 * __ldg(pb + (i >> 3)) + (i & 7) : i; };
-    if (n <= p.k) {                                          // (the same for the whole cluster)
-        if (rank == 0) {
-            for (int i = tid; i < n; i += kSelThreads) out[i] = pos_of(i);
-            if (tid == 0) p.cnt_out[q] = n;
-        }
-        return;
-    }
-    if (rank == 0 && tid == 0) p.cnt_out[q] = p.k;
-    const int lo = min(n, rank * slice), hi = min(n, lo + slice);
-    const int nwords = (hi - lo + 31) >> 5;
-    const int wseg = slice / 32;                             // a multiple of 128
-    const int s0 = min(hi, lo + warp * wseg), s1 = min(hi, s0 + wseg);
-
-    // a step's loads: lane l of load u holds positions st + 128 u + 4 l .. + 3
-    float4 f[kSelLoads];
-    auto load_step = [&](int st) {
-#pragma unroll
-        for (int u = 0; u < kSelLoads; ++u) {
-            const int i0 = st + 128 * u + 4 * lane;
-            if (i0 + 4 <= s1) {
-                f[u] = __ldcg(reinterpret_cast<const float4 *>(row + i0));
-            } else {
-                f[u].x = i0 < s1 ? __ldcg(row + i0) : 0.f;
-                f[u].y = i0 + 1 < s1 ? __ldcg(row + i0 + 1) : 0.f;
-                f[u].z = i0 + 2 < s1 ? __ldcg(row + i0 + 2) : 0.f;
-                f[u].w = 0.f;
-            }
-        }
-    };
-    if (s0 < s1) load_step(s0);                              // in flight while d0 is found
-
-    for (int i = tid; i < kSelMaxSlice / 32; i += kSelThreads) { sh.bits[i] = 0u; sh.ties[i] = 0u; }
-    for (int i = tid; i < 2048; i += kSelThreads) {
-        sh.h1[i] = 0u;
-        sh.hs[i] = __ldcg(p.hist0 + (int64_t)q * kBins + i);
-    }
-    for (int i = tid; i < 1024; i += kSelThreads) sh.h2[i] = 0u;
-    if (tid < 2 * kSelMaxCtas) (&sh.stat[0][0])[tid] = 0u;
-    if (tid < 4) sh.cnt[tid] = 0u;
-    __syncthreads();
-    uint32_t d0, above0;
-    pick_digit(sh.hs, kBins, (uint32_t)p.k, sh.s_warp, sh.s_res, d0, above0);
-    uint32_t k_rem = (uint32_t)p.k - above0;
-
-    // ---- the pass: keys above bin d0 into the bitmap, keys in bin d0 listed
-    // (each warp in its own region) and counted by bits 10..20
-    uint32_t wc = 0;                                         // this warp's candidates
-    for (int st = s0; st < s1; st += kSelStep) {
-        if (st != s0) load_step(st);
-#pragma unroll
-        for (int u = 0; u < kSelLoads; ++u) {
-            const int i0 = st + 128 * u + 4 * lane;
-            const uint32_t kk[4] = {score_key(f[u].x), score_key(f[u].y), score_key(f[u].z),
-                                    score_key(f[u].w)};
-            uint32_t fa = 0, fb = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool in = i0 + j < s1;
-                const uint32_t b = kk[j] >> 21;
-                fa |= (uint32_t)(in && b > d0) << j;
-                fb |= (uint32_t)(in && b == d0) << j;
-            }
-            // bitmap word (i0 - lo) / 32: the nibbles of 8 lanes
-            uint32_t wbits = fa << (4 * (lane & 7));
-            wbits |= __shfl_xor_sync(0xffffffffu, wbits, 1);
-            wbits |= __shfl_xor_sync(0xffffffffu, wbits, 2);
-            wbits |= __shfl_xor_sync(0xffffffffu, wbits, 4);
-            if ((lane & 7) == 0 && i0 < s1 && wbits) sh.bits[(i0 - lo) >> 5] = wbits;
-            // candidates: slots of this warp's region of the list, in lane order
-            const uint32_t b0 = __ballot_sync(0xffffffffu, fb & 1u), b1 = __ballot_sync(0xffffffffu, fb & 2u);
-            const uint32_t b2 = __ballot_sync(0xffffffffu, fb & 4u), b3 = __ballot_sync(0xffffffffu, fb & 8u);
-            if (b0 | b1 | b2 | b3) {
-                const uint32_t lt = (1u << lane) - 1u;
-                uint32_t slot = wc + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (fb & (1u << j)) {
-                        atomicAdd(&sh.h1[(kk[j] >> 10) & 2047u], 1u);
-                        if (slot < (uint32_t)kSelWarpCand) {
-                            sh.cand_key[warp * kSelWarpCand + slot] = kk[j];
-                            sh.cand_pos[warp * kSelWarpCand + slot] = i0 + j - lo;
-                        }
-                        ++slot;
-                    }
-                }
-                wc += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-            }
-        }
-    }
-    if (lane == 0) {
-        sh.wcnt[warp] = wc;
-        if (wc > (uint32_t)kSelWarpCand) sh.cnt[0] = 1u;     // a region overflowed
-    }
-    __syncthreads();
-    const bool listed = sh.cnt[0] == 0u;
-    // this slice's candidates, from the list or (overflow) from the score row
-    auto for_cand = [&](auto &&fn) {
-        if (listed) {
-            for (int c = tid; c < kSelCand; c += kSelThreads)
-                if ((c & (kSelWarpCand - 1)) < (int)sh.wcnt[c / kSelWarpCand]) fn(sh.cand_key[c], sh.cand_pos[c]);
-        } else {
-            for (int i = lo + tid; i < hi; i += kSelThreads) {
-                const uint32_t key = score_key(__ldcg(row + i));
-                if ((key >> 21) == d0) fn(key, i - lo);
-            }
-        }
-    };
-    // the sum over the cluster of a per-slice count table (all loads in flight together)
-    auto cluster_sum = [&](const uint32_t *tab, int i) {
-        uint32_t v[kSelMaxCtas];
-#pragma unroll
-        for (int r = 0; r < kSelMaxCtas; ++r) v[r] = r < C ? cluster.map_shared_rank(tab, r)[i] : 0u;
-        return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
-    };
-    cluster.sync();                                          // every slice's h1 is complete
-
-    // ---- bin m1 from the cluster's counts
-    const uint32_t g0 = cluster_sum(sh.h1, tid), g1 = cluster_sum(sh.h1, tid + 1024);
-    sh.hs[tid] = g0;                                         // (pick_digit above has finished with hs)
-    sh.hs[tid + 1024] = g1;
-    __syncthreads();
-    uint32_t d1, above1;
-    pick_digit(sh.hs, 2048, k_rem, sh.s_warp, sh.s_res, d1, above1);
-    k_rem -= above1;
-    const uint32_t m1 = (d0 << 11) | d1;
-    const int cap = kSelCopy / C;                            // copied keys per source slice
-    const bool copy = sh.hs[d1] <= (uint32_t)cap;            // the same in every CTA
-    // candidates above m1 join the bitmap; those in m1 are copied to every CTA
-    // (or, heavy ties, counted by their last 10 bits)
-    for_cand([&](uint32_t key, int rp) {
-        const uint32_t b = key >> 10;
-        if (b > m1) {
-            atomicOr(&sh.bits[rp >> 5], 1u << (rp & 31));
-        } else if (b == m1) {
-            if (copy) {
-                const uint32_t slot = atomicAdd(&sh.cnt[1], 1u);
-                if (slot < (uint32_t)cap)
-                    for (int r = 0; r < C; ++r) cluster.map_shared_rank(sh.copy_key, r)[rank * cap + slot] = key;
-            } else {
-                atomicAdd(&sh.h2[key & 1023u], 1u);
-            }
-        }
-    });
-    __syncthreads();
-    uint32_t T, out_base = 0, my_take = 0;
-    if (copy) {
-        uint32_t n_taken;
-        scan_sel(tid < nwords ? __popc(sh.bits[tid]) : 0u, sh.s_warp, &n_taken);
-        if (tid < C) {
-            uint32_t *t = cluster.map_shared_rank(&sh.pub[0][0], tid);
-            t[rank] = n_taken;                               // pub[0][rank]
-            t[kSelMaxCtas + rank] = sh.cnt[1];               // pub[1][rank]
-        }
-        cluster.sync();                                      // every slice's keys of m1 and counts are here
-        // T from the copied keys; per source slice, those above and equal to T
-        for (int i = tid; i < 1024; i += kSelThreads) sh.hs[i] = 0u;
-        __syncthreads();
-        for (int e = tid; e < C * cap; e += kSelThreads) {
-            const int r = e / cap;
-            if (e - r * cap < (int)sh.pub[1][r]) atomicAdd(&sh.hs[sh.copy_key[e] & 1023u], 1u);
-        }
-        __syncthreads();
-        uint32_t d2, above2;
-        pick_digit(sh.hs, 1024, k_rem, sh.s_warp, sh.s_res, d2, above2);
-        k_rem -= above2;
-        T = (m1 << 10) | d2;
-        for (int e = tid; e < C * cap; e += kSelThreads) {
-            const int r = e / cap;
-            if (e - r * cap < (int)sh.pub[1][r]) {
-                const uint32_t key = sh.copy_key[e];
-                if (key > T) atomicAdd(&sh.stat[0][r], 1u);
-                else if (key == T) atomicAdd(&sh.stat[1][r], 1u);
-            }
-        }
-        __syncthreads();
-        // this slice's keys above T and ties
-        for_cand([&](uint32_t key, int rp) {
-            if (key > T) atomicOr(&sh.bits[rp >> 5], 1u << (rp & 31));
-            else if (key == T) atomicOr(&sh.ties[rp >> 5], 1u << (rp & 31));
-        });
-        // ties are taken slice by slice in position order
-        uint32_t eq_acc = 0;
-        for (int r = 0; r < C; ++r) {
-            const uint32_t eq_r = sh.stat[1][r];
-            const uint32_t take_r = min(eq_r, k_rem > eq_acc ? k_rem - eq_acc : 0u);
-            if (r < rank) out_base += sh.pub[0][r] + sh.stat[0][r] + take_r;
-            if (r == rank) my_take = take_r;
-            eq_acc += eq_r;
-        }
-    } else {
-        cluster.sync();                                      // every slice's h2 is complete
-        sh.hs[tid] = cluster_sum(sh.h2, tid);
-        __syncthreads();
-        uint32_t d2, above2;
-        pick_digit(sh.hs, 1024, k_rem, sh.s_warp, sh.s_res, d2, above2);
-        k_rem -= above2;
-        T = (m1 << 10) | d2;
-        for_cand([&](uint32_t key, int rp) {
-            if ((key >> 10) == m1) {
-                if (key > T) {
-                    atomicOr(&sh.bits[rp >> 5], 1u << (rp & 31));
-                } else if (key == T) {
-                    atomicOr(&sh.ties[rp >> 5], 1u << (rp & 31));
-                    atomicAdd(&sh.cnt[2], 1u);
-                }
-            }
-        });
-        __syncthreads();
-        uint32_t n_taken;
-        scan_sel(tid < nwords ? __popc(sh.bits[tid]) : 0u, sh.s_warp, &n_taken);
-        if (tid < C) {
-            uint32_t *t = cluster.map_shared_rank(&sh.pub[0][0], tid);
-            t[rank] = n_taken;                               // pub[0][rank]
-            t[2 * kSelMaxCtas + rank] = sh.cnt[2];           // pub[2][rank]
-        }
-        cluster.sync();                                      // every slice's counts are here
-        uint32_t eq_acc = 0;
-        for (int r = 0; r < C; ++r) {
-            const uint32_t eq_r = sh.pub[2][r];
-            const uint32_t take_r = min(eq_r, k_rem > eq_acc ? k_rem - eq_acc : 0u);
-            if (r < rank) out_base += sh.pub[0][r] + take_r;
-            if (r == rank) my_take = take_r;
-            eq_acc += eq_r;
-        }
-    }
-    // (no shared memory of a peer is touched past the last cluster barrier)
-    __syncthreads();
-    // this slice's first my_take ties join its taken positions, which are
-    // written ascending from out_base
-    const uint32_t wt = tid < nwords ? sh.ties[tid] : 0u;
-    const uint32_t tb = scan_sel(__popc(wt), sh.s_warp, nullptr);
-    uint32_t w = tid < nwords ? sh.bits[tid] : 0u;
-    if (tb < my_take) {
-        uint32_t need = my_take - tb, x = wt;
-        while (x && need) {
-            const uint32_t lowbit = x & (~x + 1u);
-            w |= lowbit;
-            x ^= lowbit;
-            --need;
-        }
-    }
-    uint32_t o = out_base + scan_sel(__popc(w), sh.s_warp, nullptr);
-    while (w) {
-        const int b = __ffs(w) - 1;
-        w &= w - 1u;
-        if (o < (uint32_t)p.k) out[o] = pos_of(lo + 32 * tid + b);
-        ++o;
-    }
-}
-
 // Pool size: 8 per chosen block, minus the invisible tail of the newest block
 // when it is partial and was chosen.
 __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
@@ -950,10 +572,9 @@ size_t topk_workspace_bytes(int nq, int64_t max_n)
 cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid, int n_div8,
                         const int32_t *pool_blk, int pool_blocks, int nq, int64_t max_n, int k,
                         int32_t *idx_out, int64_t ld_idx, int32_t *cnt_out, void *ws,
-                        const uint32_t *hist0, cudaStream_t st)
+                        cudaStream_t st)
 {
     TopkParams p{};
-    p.hist0 = hist0;
     p.scores = scores;
     p.ld = ld;
     p.n_valid = n_valid;
@@ -978,21 +599,6 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     w += align_up((size_t)nq * ws_chunks * 8, 256);
     p.coff = reinterpret_cast<uint32_t *>(w);
 
-    if (hist0 != nullptr && topk_select_fits(max_n, k)) {
-        // C CTAs per query (a power of two, at most 8, about 16K positions each),
-        // each a slice of a multiple of 4,096 positions (warp segments of a
-        // multiple of 128), at most 32,768 (one bitmap word per thread)
-        int C = 1;
-        while (C < kSelMaxCtas && (int64_t)(2 * C) * kSelSlice <= max_n) C *= 2;
-        const int64_t per = (max_n + C - 1) / C;
-        const int slice = (int)((per + 4095) / 4096 * 4096);
-        static_assert(kSelMaxSlice / 32 <= kSelThreads, "one bitmap word per thread");
-        const size_t smem = sizeof(SelShared);
-        cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const cudaError_t e = launch_k(topk_select_kernel, dim3(C, nq), dim3(kSelThreads), smem, st,
-                                       (unsigned)C, p, slice);
-        return e != cudaSuccess ? e : cudaGetLastError();
-    }
     if (max_n <= kClusterMax) {
         const int chunk = (int)(((max_n + kClusterCtas - 1) / kClusterCtas + 3) & ~3);
         const size_t smem = (size_t)chunk * 4;
@@ -1015,8 +621,6 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-bool topk_select_fits(int64_t max_n, int k) { return max_n <= kSelMaxN && k >= 1; }
-
 cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_valid, int nq,
                         int64_t max_n, int pool_blocks, int32_t *pool_blk, int32_t *pool_n,
                         void *ws, cudaStream_t st)
@@ -1024,7 +628,7 @@ cudaError_t launch_pool(const float *blockmax, int64_t ld_bm, const int32_t *n_v
     // the counts of chosen blocks go to pool_n first, then become positions
     const int64_t max_blocks = (max_n + 7) / 8;
     cudaError_t e = launch_topk(blockmax, ld_bm, n_valid, 1, nullptr, 0, nq, max_blocks,
-                                pool_blocks, pool_blk, pool_blocks, pool_n, ws, nullptr, st);
+                                pool_blocks, pool_blk, pool_blocks, pool_n, ws, st);
     if (e != cudaSuccess) return e;
     e = launch_k(pool_count_kernel, dim3((nq + 127) / 128), dim3(128), 0, st, 0,
                  (const int32_t *)n_valid, (const int32_t *)pool_blk, pool_blocks,
@@ -1090,7 +694,7 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t ld_scores,
     if (scratch == nullptr) return CSA2_ERR_CUDA;
     // launch_topk's first kernel clears the histograms and state it reads later
     const cudaError_t e = launch_topk(scores, ld_scores, n_valid, 0, pool_blk, pool_blocks, nq,
-                                      max_n, k, idx_out, ld_idx, cnt_out, scratch, nullptr,
+                                      max_n, k, idx_out, ld_idx, cnt_out, scratch,
                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }

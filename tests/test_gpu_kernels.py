@@ -614,13 +614,11 @@ def test_attention_peaky_logits_rescale_and_split_merge(layout):
 # ---------------------------------------------------------------- layer top-k under heavy ties
 @pytest.mark.parametrize("distinct", [1, 3, 400, 2000])
 def test_layer_full_topk_with_few_distinct_scores(distinct):
-    # Inside csa2_layer_step a decode Full layer's indexer counts the top-k's
-    # first radix digit and a cluster per query selects from it; with every
-    # entry's key one of `distinct` integer vectors, scores tie by the tens of
-    # thousands (1, 3: the threshold bin exceeds the selection's candidate list
-    # and its copy area) or by the tens to hundreds (400, 2000: ties at the k-th
-    # score in both slices of the row), and the lowest positions must win among
-    # equal scores.
+    # A decode Full layer's top-k inside csa2_layer_step, with every entry's key
+    # one of `distinct` integer vectors: scores tie by the tens of thousands
+    # (1, 3: the threshold bin holds most of the row) or by the tens to
+    # hundreds (400, 2000: ties at the k-th score spread over the row), and the
+    # lowest positions must win among equal scores.
     n_ent, B, k = 40000, 2, 2048
     wl = ci.Workload("t", B, [n_ent] * B, 0, 1, exact=True, seed=41)
     cache = csa.Cache([n_ent + 8] * B, wl.d_idx, 1, DEV)
