@@ -43,7 +43,10 @@
 // splits of a query (at most 8) form a thread-block cluster: every CTA sends
 // its reference max and sum to all peers, scales its O^T by 2^(m_s - M) / L
 // and stores each 32-channel chunk into the shared memory of the CTA that owns
-// the chunk, which sums the splits' chunks and writes the output.  Nothing
+// the chunk ([64 heads][32 channels]; a 4 x 4 transpose within each group of 4
+// lanes gives a lane 4 channels of one head, so a warp store writes four
+// contiguous 128-byte head rows in 16-byte words), which sums the splits'
+// chunks and writes the output 16 bytes at a time.  Nothing
 // goes through global memory between splits.  The set-up that reads nothing
 // the previous kernel writes (barriers, TMEM, and inside a layer step the
 // query block and the query's metadata) runs before the
@@ -242,6 +245,21 @@ __device__ __forceinline__ int tc_row_count(const AttnParams &p, int q)
 // split, [64 heads][32 channels] fp32 (8 KB), so that a warp (lane = channel)
 // writes and reads 128 contiguous bytes per head.
 constexpr int kXBlock = 64 * 32;
+
+// 4 x 4 transpose within each group of 4 lanes: lane 4g + j holds a[i] =
+// element (row j, column i) before and element (row i, column j) after.
+__device__ __forceinline__ void transpose4(float (&a)[4], int lane)
+{
+    const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
+    float x0 = b0 ? a[0] : a[1], x1 = b0 ? a[2] : a[3];
+    float r0 = __shfl_xor_sync(0xffffffffu, x0, 1), r1 = __shfl_xor_sync(0xffffffffu, x1, 1);
+    if (b0) { a[0] = r0; a[2] = r1; } else { a[1] = r0; a[3] = r1; }
+    x0 = b1 ? a[0] : a[2];
+    x1 = b1 ? a[1] : a[3];
+    r0 = __shfl_xor_sync(0xffffffffu, x0, 2);
+    r1 = __shfl_xor_sync(0xffffffffu, x1, 2);
+    if (b1) { a[0] = r0; a[1] = r1; } else { a[2] = r0; a[3] = r1; }
+}
 constexpr int kMaxClusterSplits = 8;
 
 __device__ __forceinline__ void cluster_arrive()
@@ -758,39 +776,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
                     for (int h = 0; h < 16; ++h) o[h] = 0.f;
                 }
                 const int c = 4 * mb + (int)quarter;
-                if (S == 1) {
-                    // a single split: its scaled O^T is the output (lane = channel)
-                    float *od = p.out + ((int64_t)q * H + h0) * CSA2_D + 32 * c + lane;
+                // lane 4g + j: channels 32c + 4g .. + 3 of head h0 + 4k + j, one
+                // 16-byte word (8 lanes write one head's 128 contiguous bytes)
+                const int g4 = 4 * (lane >> 2), j = lane & 3;
+                float *dst = S == 1 ? nullptr
+                                    : cluster.map_shared_rank(sX, c % S) + ((c / S) * S + rank) * kXBlock;
 #pragma unroll
-                    for (int h = 0; h < 16; ++h)
-                        if (h0 + h < H) od[(int64_t)h * CSA2_D] = o[h] * f[h];
-                    continue;
+                for (int k = 0; k < 4; ++k) {
+                    float a[4] = {o[4 * k] * f[4 * k], o[4 * k + 1] * f[4 * k + 1],
+                                  o[4 * k + 2] * f[4 * k + 2], o[4 * k + 3] * f[4 * k + 3]};
+                    transpose4(a, lane);
+                    const int h = h0 + 4 * k + j;
+                    const float4 v = make_float4(a[0], a[1], a[2], a[3]);
+                    if (S == 1) {
+                        // a single split: its scaled O^T is the output
+                        if (h < H)
+                            *reinterpret_cast<float4 *>(p.out + ((int64_t)q * H + h) * CSA2_D + 32 * c + g4) = v;
+                    } else {
+                        *reinterpret_cast<float4 *>(dst + h * 32 + g4) = v;
+                    }
                 }
-                float *dst = cluster.map_shared_rank(sX, c % S) +
-                             ((c / S) * S + rank) * kXBlock + h0 * 32 + lane;
-#pragma unroll
-                for (int h = 0; h < 16; ++h) dst[h * 32] = o[h] * f[h];
             }
         }
         if (S > 1) cluster.sync();   // every block has arrived at its owner (S is uniform)
-        // chunks rank, rank + S, ...: lane = channel; a warp sums 4 heads per item
-        // (all their loads in flight together)
+        // chunks rank, rank + S, ...: a warp sums 4 heads of the chunk per item,
+        // lane 8j + g4 / 4 the channels g4 .. g4 + 3 of head hb + j (one 16-byte
+        // load per split, all in flight; one 16-byte store)
         const int n_own = S > 1 ? (16 - rank + S - 1) / S : 0;
         for (int it = warp; it < n_own * 16; it += kTcThreads / 32) {
-            const int k = it >> 4, hb = 4 * (it & 15), c = rank + k * S;
-            if (hb >= H) continue;
-            const float *src = sX + k * S * kXBlock + hb * 32 + lane;
-            float v[4][kMaxClusterSplits];
+            const int k = it >> 4, c = rank + k * S;
+            const int h = 4 * (it & 15) + (lane >> 3), g4 = 4 * (lane & 7);
+            if (h >= H) continue;
+            const float *src = sX + k * S * kXBlock + h * 32 + g4;
+            float4 v[kMaxClusterSplits];
 #pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[j][s] = (s < S) ? src[s * kXBlock + j * 32] : 0.f;
-            float *od = p.out + ((int64_t)q * H + hb) * CSA2_D + 32 * c + lane;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (hb + j < H)
-                    od[(int64_t)j * CSA2_D] = ((v[j][0] + v[j][1]) + (v[j][2] + v[j][3])) +
-                                              ((v[j][4] + v[j][5]) + (v[j][6] + v[j][7]));
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+                v[s2] = (s2 < S) ? *reinterpret_cast<const float4 *>(src + s2 * kXBlock)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 r;
+            r.x = ((v[0].x + v[1].x) + (v[2].x + v[3].x)) + ((v[4].x + v[5].x) + (v[6].x + v[7].x));
+            r.y = ((v[0].y + v[1].y) + (v[2].y + v[3].y)) + ((v[4].y + v[5].y) + (v[6].y + v[7].y));
+            r.z = ((v[0].z + v[1].z) + (v[2].z + v[3].z)) + ((v[4].z + v[5].z) + (v[6].z + v[7].z));
+            r.w = ((v[0].w + v[1].w) + (v[2].w + v[3].w)) + ((v[4].w + v[5].w) + (v[6].w + v[7].w));
+            *reinterpret_cast<float4 *>(p.out + ((int64_t)q * H + h) * CSA2_D + 32 * c + g4) = r;
         }
     }
 
