@@ -327,10 +327,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         mbar_arrive_expect_tx(bar_q, qbytes);
         bulk_load(sV, p.q + (int64_t)q * H * CSA2_D, qbytes, bar_q);
     };
+    // ---- Q: the raw bf16 block [H][512] lands in the V tile, then bf16 -> f16 into
+    // the K-major 128-byte-swizzled sQ (heads >= H are zero): inside a layer
+    // step while the top-k finishes, otherwise while the first tile's rows are
+    // in flight (the first tile's stores into the V tile come after a barrier)
+    auto convert_q = [&]() {
+        volatile int no_abort = 0;
+        if (!mbar_wait(bar_q, 0, &no_abort)) sFlag[0] = 1;
+        for (int i = tid; i < kHeads * (CSA2_D / 8); i += kTcThreads) {
+            const int h = i / (CSA2_D / 8), c8 = i % (CSA2_D / 8);   // 8 channels per chunk
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (h < H) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sV + h * 1024 + c8 * 16);
+                v = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
+                               bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
+            }
+            *reinterpret_cast<uint4 *>(sQ + (c8 >> 3) * kQAtom + sw128(h, c8 & 7)) = v;
+        }
+    };
     if (tid == 0 && p.early) load_q();
     if (warp == 0) { tmem_alloc(sTmem, 512); tmem_relinquish(); }
     TcRowSet rs{};
-    if (p.early) rs = tc_row_set(p, q);
+    if (p.early) {
+        rs = tc_row_set(p, q);
+        convert_q();
+    }
     pdl_wait();
     pdl_trigger();
     if (tid == 0 && !p.early) load_q();
@@ -466,23 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
         if (n_tiles > 1) gj = rows_entry(1);
         if (n_tiles > 2) gj2 = rows_entry(2);
     }
-    // ---- Q: the raw bf16 block [H][512] lands in the V tile, then bf16 -> f16 into
-    // the K-major 128-byte-swizzled sQ (heads >= H are zero) while the first
-    // tile's rows are in flight
-    {
-        volatile int no_abort = 0;
-        if (!mbar_wait(bar_q, 0, &no_abort)) sFlag[0] = 1;
-        for (int i = tid; i < kHeads * (CSA2_D / 8); i += kTcThreads) {
-            const int h = i / (CSA2_D / 8), c8 = i % (CSA2_D / 8);   // 8 channels per chunk
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (h < H) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(sV + h * 1024 + c8 * 16);
-                v = make_uint4(bf16x2_to_f16x2(raw.x), bf16x2_to_f16x2(raw.y),
-                               bf16x2_to_f16x2(raw.z), bf16x2_to_f16x2(raw.w));
-            }
-            *reinterpret_cast<uint4 *>(sQ + (c8 >> 3) * kQAtom + sw128(h, c8 & 7)) = v;
-        }
-    }
+    // (p.early: the query was converted before the dependent-launch wait)
+    if (!p.early) convert_q();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
