@@ -538,6 +538,399 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClThread
     }
 }
 
+// ---------------------------------------------------------------- one CTA per query
+// One CTA of 512 threads per query (rows up to kRsMaxN candidates), no
+// cluster: used when a launch has enough queries to fill the GPU, or few
+// enough rows that one CTA each finishes before a cluster would.  A strided
+// sample of about 4,096 keys gives, by two radix rounds over the sample, a
+// 22-bit threshold with about 1.5 k / stride + 16 sampled keys above it; one
+// pass over the row lists every key at or above it with its position, in
+// per-warp regions of the list.  That list holds the top k whenever it holds
+// at least k keys; three radix rounds over the list alone give the exact k-th
+// key T, the list's keys above T go to a bitmap of positions and its keys
+// equal to T to a tie bitmap, of which the lowest positions are taken, and the
+// set bits are written in ascending order.  With stride 1 (rows up to 4,096)
+// the threshold is exact.  When the list overflows a region or holds fewer
+// than k keys (heavy ties, an unlucky sample), an exact path takes over: a full
+// count of the top 11 bits, a pass that marks the keys above that bin and
+// lists the bin's keys, two rounds over that list (or over the row again when
+// it overflows).
+constexpr int kRsThreads = 512;
+constexpr int kRsWarps = kRsThreads / 32;
+constexpr int kRsMaxN = 262144;
+constexpr int kRsWords = kRsMaxN / 32;              // 8,192 bitmap words: 512 per warp
+constexpr int kRsCand = 8192;                       // list entries: 512 per warp
+constexpr int kRsWarpCand = kRsCand / kRsWarps;
+constexpr int kRsSample = 4096;
+constexpr int kRsMinQueries = 96;
+constexpr int kRsLoads = 8;                         // 16-byte loads per lane in flight
+
+struct RsShared {
+    uint32_t bits[kRsWords];      // taken positions
+    uint32_t ties[kRsWords];      // positions whose key equals T
+    uint32_t cand_key[kRsCand];
+    int32_t cand_pos[kRsCand];
+    uint32_t hist[kBins];
+    uint32_t wcnt[kRsWarps];      // list entries of each warp (fast path)
+    uint32_t s_warp[kRsWarps];
+    uint32_t s_res[2];
+    uint32_t n_cand;
+    uint32_t flag;                // a warp's list region overflowed
+};
+
+// The digit d of a round over bins h[0 .. nb) (from the top): count(> d) < need
+// <= count(>= d); every thread gets d and count(> d) (0, 0 when the bins hold
+// fewer than need).  512 threads, 4 bins each.
+__device__ __forceinline__ void rs_pick(const uint32_t *h, int nb, uint32_t need, uint32_t *s_warp,
+                                        uint32_t *s_res, uint32_t &d, uint32_t &above)
+{
+    const int tid = threadIdx.x;
+    uint32_t c[4], mine = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int b = nb - 1 - 4 * tid - j;
+        c[j] = b >= 0 ? h[b] : 0u;
+        mine += c[j];
+    }
+    if (tid == 0) { s_res[0] = 0u; s_res[1] = 0u; }
+    const uint32_t before = scan512(mine, s_warp, nullptr);
+    if (before < need && need <= before + mine) {
+        uint32_t acc = before;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (need <= acc + c[j]) { s_res[0] = (uint32_t)(nb - 1 - 4 * tid - j); s_res[1] = acc; break; }
+            acc += c[j];
+        }
+    }
+    __syncthreads();
+    d = s_res[0];
+    above = s_res[1];
+    __syncthreads();
+}
+
+// Warp-inclusive scan
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+__global__ void __launch_bounds__(kRsThreads, 1) topk_rowselect_kernel(TopkParams p)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) uint8_t rs_smem[];
+    RsShared &sh = *reinterpret_cast<RsShared *>(rs_smem);
+    const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int n = p.n_valid[q];
+    if (p.n_div8) n = (n + 7) / 8;
+    if (n < 0) n = 0;
+    if (n > p.max_n) n = (int)p.max_n;
+    const float *row = p.scores + (int64_t)q * p.ld;
+    int32_t *out = p.idx_out + (int64_t)q * p.ld_idx;
+    const int32_t *pb = p.pool_blk ? p.pool_blk + (int64_t)q * p.pool_blocks : nullptr;
+    auto pos_of = [&](int i) { return pb ? 8 * __ldg(pb + (i >> 3)) + (i & 7) : i; };
+    if (n <= p.k) {
+        for (int i = tid; i < n; i += kRsThreads) out[i] = pos_of(i);
+        if (tid == 0) p.cnt_out[q] = n;
+        return;
+    }
+    if (tid == 0) p.cnt_out[q] = p.k;
+    const int nwords = (n + 31) >> 5;
+    for (int i = tid; i < kRsWords; i += kRsThreads) { sh.bits[i] = 0u; sh.ties[i] = 0u; }
+    for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+    if (tid == 0) { sh.n_cand = 0u; sh.flag = 0u; }
+    // a warp's pieces of the row (below): the first one's loads go out now
+    auto load_piece = [&](float4 (&f)[kRsLoads], int base) {
+#pragma unroll
+        for (int u = 0; u < kRsLoads; ++u) {
+            const int i0 = base + 128 * u + 4 * lane;
+            if (i0 + 4 <= n) {
+                f[u] = __ldcg(reinterpret_cast<const float4 *>(row + i0));
+            } else {
+                f[u].x = i0 < n ? __ldcg(row + i0) : 0.f;
+                f[u].y = i0 + 1 < n ? __ldcg(row + i0 + 1) : 0.f;
+                f[u].z = i0 + 2 < n ? __ldcg(row + i0 + 2) : 0.f;
+                f[u].w = 0.f;
+            }
+        }
+    };
+    constexpr int kStride = 1024 * kRsWarps;
+    float4 fa[kRsLoads], fb[kRsLoads];
+    if (1024 * warp < n) load_piece(fa, 1024 * warp);
+
+    // ---- the sample: positions st * m, m < n_s (8 per thread at most)
+    const int st = (n + kRsSample - 1) / kRsSample;
+    const int n_s = (n + st - 1) / st;
+    uint32_t smp[kRsSample / kRsThreads];
+#pragma unroll
+    for (int j = 0; j < kRsSample / kRsThreads; ++j) {
+        const int m = tid + kRsThreads * j;
+        smp[j] = m < n_s ? score_key(__ldcg(row + (int64_t)m * st)) : 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRsSample / kRsThreads; ++j)
+        if (tid + kRsThreads * j < n_s) atomicAdd(&sh.hist[smp[j] >> 21], 1u);
+    __syncthreads();
+    // keys above the threshold, counted in the sample: k exactly when the sample
+    // is the row, else about 1.5 k / st + 16
+    const uint32_t t_s = st == 1 ? (uint32_t)p.k : min((uint32_t)n_s, (uint32_t)((3LL * p.k) / (2LL * st)) + 16u);
+    uint32_t da, above;
+    rs_pick(sh.hist, kBins, t_s, sh.s_warp, sh.s_res, da, above);
+    for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRsSample / kRsThreads; ++j)
+        if (tid + kRsThreads * j < n_s && (smp[j] >> 21) == da) atomicAdd(&sh.hist[(smp[j] >> 10) & 2047u], 1u);
+    __syncthreads();
+    uint32_t db;
+    rs_pick(sh.hist, kBins, t_s - above, sh.s_warp, sh.s_res, db, above);
+    const uint32_t key_lo = (da << 21) | (db << 10);   // list: keys >= key_lo
+
+    // ---- the list pass: warp w takes the 1,024-position pieces w, w + 16, ...
+    // (lane l of load u: positions 128 u + 4 l .. + 3), the next piece's loads in
+    // flight while one is processed.  A lane's 32 decisions of a piece form one
+    // mask (bit 4u + j), one warp scan gives the lane its slots in the warp's
+    // region, and the positions of its keys >= key_lo are stored (their keys are
+    // read back from the row after the pass)
+    uint32_t wc = 0;
+    auto list_piece = [&](const float4 (&f)[kRsLoads], int base) {
+        uint32_t mask = 0;
+#pragma unroll
+        for (int u = 0; u < kRsLoads; ++u) {
+            const int i0 = base + 128 * u + 4 * lane;
+            mask |= (uint32_t)(i0 < n && score_key(f[u].x) >= key_lo) << (4 * u);
+            mask |= (uint32_t)(i0 + 1 < n && score_key(f[u].y) >= key_lo) << (4 * u + 1);
+            mask |= (uint32_t)(i0 + 2 < n && score_key(f[u].z) >= key_lo) << (4 * u + 2);
+            mask |= (uint32_t)(i0 + 3 < n && score_key(f[u].w) >= key_lo) << (4 * u + 3);
+        }
+        const uint32_t cb = __popc(mask);
+        const uint32_t incl = warp_incl_scan(cb, lane);
+        uint32_t slot = wc + incl - cb;
+        while (mask) {
+            const int bit = __ffs(mask) - 1;
+            mask &= mask - 1u;
+            if (slot < (uint32_t)kRsWarpCand)
+                sh.cand_pos[warp * kRsWarpCand + slot] = base + 128 * (bit >> 2) + 4 * lane + (bit & 3);
+            ++slot;
+        }
+        wc += __shfl_sync(0xffffffffu, incl, 31);
+    };
+    for (int base = 1024 * warp; base < n; base += 2 * kStride) {
+        if (base + kStride < n) load_piece(fb, base + kStride);
+        list_piece(fa, base);
+        if (base + 2 * kStride < n) load_piece(fa, base + 2 * kStride);
+        if (base + kStride < n) list_piece(fb, base + kStride);
+    }
+    // the listed keys, read back from the row (one load each, all in flight)
+    for (int s2 = lane; s2 < (int)min(wc, (uint32_t)kRsWarpCand); s2 += 32)
+        sh.cand_key[warp * kRsWarpCand + s2] = score_key(__ldcg(row + sh.cand_pos[warp * kRsWarpCand + s2]));
+    if (lane == 0) {
+        sh.wcnt[warp] = wc;
+        if (wc > (uint32_t)kRsWarpCand) sh.flag = 1u;
+    }
+    __syncthreads();
+    uint32_t c_total = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) c_total += sh.wcnt[w];
+    const bool fast = sh.flag == 0u && c_total >= (uint32_t)p.k;
+    uint32_t T, k_rem, d0, d1, d2;
+    if (fast) {
+        // ---- three radix rounds over the list alone
+        auto for_list = [&](auto &&fn) {
+            for (int e = tid; e < kRsCand; e += kRsThreads)
+                if ((e % kRsWarpCand) < (int)sh.wcnt[e / kRsWarpCand]) fn(sh.cand_key[e], sh.cand_pos[e]);
+        };
+        for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        for_list([&](uint32_t key, int) { atomicAdd(&sh.hist[key >> 21], 1u); });
+        __syncthreads();
+        rs_pick(sh.hist, kBins, (uint32_t)p.k, sh.s_warp, sh.s_res, d0, above);
+        k_rem = (uint32_t)p.k - above;
+        for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        for_list([&](uint32_t key, int) {
+            if ((key >> 21) == d0) atomicAdd(&sh.hist[(key >> 10) & 2047u], 1u);
+        });
+        __syncthreads();
+        rs_pick(sh.hist, kBins, k_rem, sh.s_warp, sh.s_res, d1, above);
+        k_rem -= above;
+        const uint32_t m1 = (d0 << 11) | d1;
+        for (int i = tid; i < 1024; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        for_list([&](uint32_t key, int) {
+            if ((key >> 10) == m1) atomicAdd(&sh.hist[key & 1023u], 1u);
+        });
+        __syncthreads();
+        rs_pick(sh.hist, 1024, k_rem, sh.s_warp, sh.s_res, d2, above);
+        k_rem -= above;                                  // keys equal to T that are taken
+        T = (m1 << 10) | d2;
+        for_list([&](uint32_t key, int pos) {
+            if (key > T) atomicOr(&sh.bits[pos >> 5], 1u << (pos & 31));
+            else if (key == T) atomicOr(&sh.ties[pos >> 5], 1u << (pos & 31));
+        });
+    } else {
+        // ---- exact path.  Pass 1: count of the top 11 key bits
+        for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        for (int i0 = 4 * tid; i0 < n; i0 += 4 * kRsThreads * kRsLoads) {
+            float4 f[kRsLoads];
+#pragma unroll
+            for (int u = 0; u < kRsLoads; ++u) {
+                const int i = i0 + 4 * kRsThreads * u;
+                if (i + 4 <= n) f[u] = __ldcg(reinterpret_cast<const float4 *>(row + i));
+            }
+#pragma unroll
+            for (int u = 0; u < kRsLoads; ++u) {
+                const int i = i0 + 4 * kRsThreads * u;
+                if (i + 4 <= n) {
+                    atomicAdd(&sh.hist[score_key(f[u].x) >> 21], 1u);
+                    atomicAdd(&sh.hist[score_key(f[u].y) >> 21], 1u);
+                    atomicAdd(&sh.hist[score_key(f[u].z) >> 21], 1u);
+                    atomicAdd(&sh.hist[score_key(f[u].w) >> 21], 1u);
+                } else {
+                    for (int j = i; j < n; ++j) atomicAdd(&sh.hist[score_key(__ldcg(row + j)) >> 21], 1u);
+                }
+            }
+        }
+        __syncthreads();
+        rs_pick(sh.hist, kBins, (uint32_t)p.k, sh.s_warp, sh.s_res, d0, above);
+        k_rem = (uint32_t)p.k - above;
+        for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        // pass 2: keys above bin d0 into the bitmap (lanes 8j .. 8j + 7 make one
+        // word), keys in bin d0 listed (shared slot counter) and counted by bits 10..20
+        for (int base = 1024 * warp; base < n; base += 1024 * kRsWarps) {
+            float4 f[kRsLoads];
+#pragma unroll
+            for (int u = 0; u < kRsLoads; ++u) {
+                const int i0 = base + 128 * u + 4 * lane;
+                if (i0 + 4 <= n) {
+                    f[u] = __ldcg(reinterpret_cast<const float4 *>(row + i0));
+                } else {
+                    f[u].x = i0 < n ? __ldcg(row + i0) : 0.f;
+                    f[u].y = i0 + 1 < n ? __ldcg(row + i0 + 1) : 0.f;
+                    f[u].z = i0 + 2 < n ? __ldcg(row + i0 + 2) : 0.f;
+                    f[u].w = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRsLoads; ++u) {
+                const int i0 = base + 128 * u + 4 * lane;
+                const uint32_t kk[4] = {score_key(f[u].x), score_key(f[u].y), score_key(f[u].z),
+                                        score_key(f[u].w)};
+                uint32_t fa = 0, fb = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = i0 + j < n;
+                    fa |= (uint32_t)(in && (kk[j] >> 21) > d0) << j;
+                    fb |= (uint32_t)(in && (kk[j] >> 21) == d0) << j;
+                }
+                uint32_t wbits = fa << (4 * (lane & 7));
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 1);
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 2);
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 4);
+                if ((lane & 7) == 0 && i0 < n && wbits) sh.bits[i0 >> 5] = wbits;
+                if (__ballot_sync(0xffffffffu, fb != 0u)) {
+                    const uint32_t cb = __popc(fb);
+                    const uint32_t incl = warp_incl_scan(cb, lane);
+                    uint32_t slot = 0;
+                    if (lane == 31) slot = atomicAdd(&sh.n_cand, incl);
+                    slot = __shfl_sync(0xffffffffu, slot, 31) + incl - cb;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (fb & (1u << j)) {
+                            atomicAdd(&sh.hist[(kk[j] >> 10) & 2047u], 1u);
+                            if (slot < (uint32_t)kRsCand) {
+                                sh.cand_key[slot] = kk[j];
+                                sh.cand_pos[slot] = i0 + j;
+                            }
+                            ++slot;
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        const bool listed = sh.n_cand <= (uint32_t)kRsCand;
+        const int n_cand = listed ? (int)sh.n_cand : 0;
+        // the keys of bin d0, from the list or (overflow) from the row
+        auto for_cand = [&](auto &&fn) {
+            if (listed) {
+                for (int c = tid; c < n_cand; c += kRsThreads) fn(sh.cand_key[c], sh.cand_pos[c]);
+            } else {
+                for (int i = tid; i < n; i += kRsThreads) {
+                    const uint32_t key = score_key(__ldcg(row + i));
+                    if ((key >> 21) == d0) fn(key, i);
+                }
+            }
+        };
+        rs_pick(sh.hist, kBins, k_rem, sh.s_warp, sh.s_res, d1, above);
+        k_rem -= above;
+        const uint32_t m1 = (d0 << 11) | d1;
+        for (int i = tid; i < 1024; i += kRsThreads) sh.hist[i] = 0u;
+        __syncthreads();
+        for_cand([&](uint32_t key, int) {
+            if ((key >> 10) == m1) atomicAdd(&sh.hist[key & 1023u], 1u);
+        });
+        __syncthreads();
+        rs_pick(sh.hist, 1024, k_rem, sh.s_warp, sh.s_res, d2, above);
+        k_rem -= above;
+        T = (m1 << 10) | d2;
+        for_cand([&](uint32_t key, int pos) {
+            if (key > T) atomicOr(&sh.bits[pos >> 5], 1u << (pos & 31));
+            else if (key == T) atomicOr(&sh.ties[pos >> 5], 1u << (pos & 31));
+        });
+    }
+    __syncthreads();
+
+    // ---- output.  Thread t owns bitmap words 16t .. 16t + 15 (ascending
+    // positions; four 16-byte reads).  Ties are taken in position order: the
+    // threads before it take theirs first.
+    const int w0 = 16 * tid;
+    uint32_t bw[16], tw[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 b4 = reinterpret_cast<const uint4 *>(sh.bits + w0)[v];
+        const uint4 t4 = reinterpret_cast<const uint4 *>(sh.ties + w0)[v];
+        bw[4 * v] = b4.x; bw[4 * v + 1] = b4.y; bw[4 * v + 2] = b4.z; bw[4 * v + 3] = b4.w;
+        tw[4 * v] = t4.x; tw[4 * v + 1] = t4.y; tw[4 * v + 2] = t4.z; tw[4 * v + 3] = t4.w;
+    }
+    uint32_t n_tie = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) n_tie += __popc(tw[j]);
+    const uint32_t ties_before = scan512(n_tie, sh.s_warp, nullptr);
+    uint32_t keep = k_rem > ties_before ? min(n_tie, k_rem - ties_before) : 0u;
+    uint32_t n_sel = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint32_t t = tw[j];
+        while (t && keep) {
+            const uint32_t low = t & (~t + 1u);
+            bw[j] |= low;
+            t ^= low;
+            --keep;
+        }
+        n_sel += __popc(bw[j]);
+    }
+    uint32_t o = scan512(n_sel, sh.s_warp, nullptr);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint32_t x = bw[j];
+        while (x) {
+            const int bit = __ffs(x) - 1;
+            x &= x - 1u;
+            if (o < (uint32_t)p.k) out[o] = pos_of(32 * (w0 + j) + bit);
+            ++o;
+        }
+    }
+}
+
 // Pool size: 8 per chosen block, minus the invisible tail of the newest block
 // when it is partial and was chosen.
 __global__ void pool_count_kernel(const int32_t *n_valid, const int32_t *pool_blk, int pool_blocks,
@@ -599,6 +992,12 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const int32_t *n_valid,
     w += align_up((size_t)nq * ws_chunks * 8, 256);
     p.coff = reinterpret_cast<uint32_t *>(w);
 
+    if (nq >= kRsMinQueries && max_n <= kRsMaxN) {
+        const size_t smem = sizeof(RsShared);
+        cudaFuncSetAttribute(topk_rowselect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = launch_k(topk_rowselect_kernel, dim3(nq), dim3(kRsThreads), smem, st, 0, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     if (max_n <= kClusterMax) {
         const int chunk = (int)(((max_n + kClusterCtas - 1) / kClusterCtas + 3) & ~3);
         const size_t smem = (size_t)chunk * 4;

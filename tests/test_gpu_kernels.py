@@ -382,6 +382,35 @@ def test_topk_all_equal_and_few_distinct(n):
         assert cnt[i] == k and np.array_equal(idx[i, :k], ref), i
 
 
+@pytest.mark.parametrize("n,k", [(70001, 2048), (262144, 2048), (9000, 4096)])
+def test_topk_many_queries_bit_exact(n, k):
+    # at least 96 queries in one call (a prefill chunk) take one CTA per query;
+    # rows of every kind in one launch: random floats, heavy ties, all equal,
+    # n <= k, three distinct values (the threshold bin exceeds the candidate
+    # list), negative and positive zero, a ragged tail
+    nq = 100
+    rng = np.random.default_rng(n + 7 * k)
+    s = rng.normal(size=(nq, n)).astype(np.float32)
+    nvalid = []
+    for i in range(nq):
+        kind = i % 6
+        if kind == 1:
+            s[i] = np.round(s[i] * 4) / 4
+        elif kind == 2:
+            s[i] = 1.5
+        elif kind == 4:
+            s[i] = rng.choice(np.array([0.25, 1.0, 3.0], np.float32), size=n)
+        elif kind == 5:
+            s[i, ::5] = 0.0
+            s[i, 2::5] = -0.0
+        nvalid.append(int(rng.integers(1, k + 1)) if kind == 3 else n - int(rng.integers(0, 40)))
+    idx, cnt = _topk_gpu(s, nvalid, k)
+    for i in range(nq):
+        ref = O.topk(s[i, :nvalid[i]], k)
+        assert cnt[i] == len(ref), i
+        assert np.array_equal(idx[i, :cnt[i]], ref), i
+
+
 def test_topk_with_pool_map():
     rng = np.random.default_rng(1)
     pool = np.sort(rng.choice(100000, 2048, replace=False)).astype(np.int32)[None].repeat(2, 0)
