@@ -16,10 +16,10 @@
 // [2^-10, 2688], so it is exact in f16 (hardware cvt.rn.f16x2.e2m1x2, then one
 // f16x2 multiply by the group scale).  Q (bf16 in) and the window rows (bf16
 // in) are converted to f16, P is stored as f16; S and O accumulate in fp32 in
-// tensor memory (64 + 256 columns).  Online softmax in base 2 with lazy
-// rescaling: the reference max of a head moves only when a tile exceeds it by
-// more than 8 (P <= 256 stays exact enough in f16), and O^T is then rescaled
-// in TMEM.
+// tensor memory (64 + 256 columns, 64 more for the running row sums).  Online
+// softmax in base 2 with lazy rescaling: the reference max of a head moves
+// only when a tile exceeds it by more than 8 (P <= 256 stays exact enough in
+// f16), and O^T is then rescaled in TMEM.
 //
 // Warps: 0..15 = workers (warp 0 also owns TMEM), 16 = MMA issuer (the
 // issuing thread stalls while the tensor pipe's queue is full, so it must not
