@@ -640,7 +640,6 @@ __global__ void __launch_bounds__(kRsThreads, 1) topk_rowselect_kernel(TopkParam
         return;
     }
     if (tid == 0) p.cnt_out[q] = p.k;
-    const int nwords = (n + 31) >> 5;
     for (int i = tid; i < kRsWords; i += kRsThreads) { sh.bits[i] = 0u; sh.ties[i] = 0u; }
     for (int i = tid; i < kBins; i += kRsThreads) sh.hist[i] = 0u;
     if (tid == 0) { sh.n_cand = 0u; sh.flag = 0u; }
