@@ -423,6 +423,47 @@ def test_topk_with_pool_map():
         assert np.array_equal(idx[i, :cnt[i]], ref)
 
 
+def test_topk_many_queries_with_pool_map():
+    # the one-CTA-per-query top-k (at least 96 queries) maps pool positions to
+    # cache positions through each query's pool blocks
+    nq, npos = 100, 16384
+    rng = np.random.default_rng(5)
+    pool = np.stack([np.sort(rng.choice(200000, 2048, replace=False)) for _ in range(nq)]).astype(np.int32)
+    pn = [npos - int(rng.integers(0, 8)) for _ in range(nq)]
+    s = np.round(rng.normal(size=(nq, npos)) * 8).astype(np.float32) / 8
+    idx, cnt = _topk_gpu(s, pn, 2048, pool=pool)
+    for i in range(nq):
+        pos = np.array([8 * pool[i, p_ // 8] + p_ % 8 for p_ in range(pn[i])], np.int32)
+        ref = O.topk(s[i, :pn[i]], 2048, pos)
+        assert np.array_equal(idx[i, :cnt[i]], ref), i
+
+
+def test_pool_select_many_queries_bit_exact():
+    # pool selection over block maxima (candidates = blocks) for 100 queries in
+    # one call, so that the one-CTA-per-query top-k picks the blocks
+    nq = 100
+    rng = np.random.default_rng(11)
+    ns = [int(rng.integers(20000, 140000)) for _ in range(nq)]
+    nbmax = (max(ns) + 7) // 8
+    bm = torch.full((nq, (nbmax + 3) // 4 * 4), -np.inf, dtype=torch.float32)
+    refs = []
+    for i, n in enumerate(ns):
+        sc = rng.normal(size=n)
+        sc[rng.integers(0, n, size=40)] = 6.0                   # ties among the largest maxima
+        rb = O.blockmax(sc)
+        bm[i, :len(rb)] = torch.from_numpy(rb.astype(np.float32))
+        refs.append(O.pool(np.repeat(rb.astype(np.float32), 8)[:n].astype(np.float64), 2048))
+    blk = torch.full((nq, 2048), -1, dtype=torch.int32, device=DEV)
+    pn = torch.zeros(nq, dtype=torch.int32, device=DEV)
+    csa.pool_select(bm.to(DEV), torch.tensor(ns, dtype=torch.int32, device=DEV), max(ns), blk, pn)
+    torch.cuda.synchronize()
+    gb, gp = _np(blk), _np(pn)
+    for i, n in enumerate(ns):
+        ref_blk, ref_pn = refs[i]
+        c = min(2048, (n + 7) // 8)
+        assert np.array_equal(gb[i, :c], ref_blk) and int(gp[i]) == ref_pn, i
+
+
 @pytest.mark.parametrize("n", [50, 16384, 16387, 200003])
 def test_pool_select_bit_exact(n):
     rng = np.random.default_rng(n)
