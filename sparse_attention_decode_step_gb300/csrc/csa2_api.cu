@@ -65,18 +65,25 @@ cudaError_t make_tmap_rows_u8(CUtensorMap *map, const void *base, int64_t rows, 
 
 // ---------------------------------------------------------------- attention plan
 // Rows of a query are processed in 128-row tiles; a query's tiles are divided
-// over `splits` CTAs (one thread-block cluster, at most 8) so that the grid
-// fills the SMs in one wave (one CTA per SM: the kernel uses ~215 KB of shared
-// memory and all 512 TMEM columns).
+// over `splits` CTAs (one thread-block cluster: at most 16 where the GPU
+// schedules clusters of 16, else 8; 13 .. 15 are not used) so that the grid
+// fills the SMs in one wave (one CTA per SM: the kernel uses ~220 KB of shared
+// memory and all 512 TMEM columns), with as few splits as give the same
+// number of tiles per split.
 int attn_plan(int nq, int k_max, int n_win)
 {
     const int rows = k_max + n_win > 0 ? k_max + n_win : 1;
     const int tiles = (rows + 127) / 128;
     const int sms = device_sm_count();
+    const int cap = attn_max_splits();
     int s = sms / (nq > 0 ? nq : 1);
     if (s > tiles) s = tiles;
-    if (s > 8) s = 8;                      // the splits of a query merge within one cluster
+    if (s > cap) s = cap;                  // the splits of a query merge within one cluster
+    if (s > 12 && s < 16) s = 12;
     if (s < 1) s = 1;
+    const int tps = (tiles + s - 1) / s;
+    s = (tiles + tps - 1) / tps;
+    if (s > 12 && s < 16) s = 16;          // (16 splits give at most tps tiles each too)
     return s;
 }
 

@@ -260,7 +260,7 @@ __device__ __forceinline__ void transpose4(float (&a)[4], int lane)
     r1 = __shfl_xor_sync(0xffffffffu, x1, 2);
     if (b1) { a[0] = r0; a[1] = r1; } else { a[2] = r0; a[3] = r1; }
 }
-constexpr int kMaxClusterSplits = 8;
+constexpr int kMaxClusterSplits = 16;   // 1 .. 12 or 16 (the receive area, below)
 
 __device__ __forceinline__ void cluster_arrive()
 {
@@ -814,16 +814,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
             const int h = 4 * (it & 15) + (lane >> 3), g4 = 4 * (lane & 7);
             if (h >= H) continue;
             const float *src = sX + k * S * kXBlock + h * 32 + g4;
-            float4 v[kMaxClusterSplits];
+            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < S; s0 += 4) {
+                float4 v[4];
 #pragma unroll
-            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-                v[s2] = (s2 < S) ? *reinterpret_cast<const float4 *>(src + s2 * kXBlock)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 r;
-            r.x = ((v[0].x + v[1].x) + (v[2].x + v[3].x)) + ((v[4].x + v[5].x) + (v[6].x + v[7].x));
-            r.y = ((v[0].y + v[1].y) + (v[2].y + v[3].y)) + ((v[4].y + v[5].y) + (v[6].y + v[7].y));
-            r.z = ((v[0].z + v[1].z) + (v[2].z + v[3].z)) + ((v[4].z + v[5].z) + (v[6].z + v[7].z));
-            r.w = ((v[0].w + v[1].w) + (v[2].w + v[3].w)) + ((v[4].w + v[5].w) + (v[6].w + v[7].w));
+                for (int j = 0; j < 4; ++j)
+                    v[j] = (s0 + j < S) ? *reinterpret_cast<const float4 *>(src + (s0 + j) * kXBlock)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                r.x += (v[0].x + v[1].x) + (v[2].x + v[3].x);
+                r.y += (v[0].y + v[1].y) + (v[2].y + v[3].y);
+                r.z += (v[0].z + v[1].z) + (v[2].z + v[3].z);
+                r.w += (v[0].w + v[1].w) + (v[2].w + v[3].w);
+            }
             *reinterpret_cast<float4 *>(p.out + ((int64_t)q * H + h) * CSA2_D + 32 * c + g4) = r;
         }
     }
@@ -836,12 +838,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p)
     }
 }
 
+// The largest cluster of attention CTAs this GPU schedules: 16 when a cluster
+// of 16 (non-portable size) fits, else the portable 8 (asked once).
+int attn_max_splits()
+{
+    static int cached = 0;
+    if (cached) return cached;
+    int m = 8;
+    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
+                            kMaxClusterSplits * 2 * 64 * 4 + 9 * 8 + 64;
+        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16, 1);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) == cudaSuccess && n > 0) m = 16;
+    }
+    cudaGetLastError();
+    cached = m;
+    return m;
+}
+
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st)
 {
-    // receive area: ceil(16 / S) chunk slots x S senders blocks, largest at S = 7 (21)
-    static_assert(21 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
+    // receive area: ceil(16 / S) chunk slots x S senders blocks, at most 24 (S = 12)
+    // for S in 1 .. 12 and 16 blocks at S = 16; S in 13 .. 15 would need 26 .. 30
+    static_assert(24 * kXBlock * 4 <= kVBytes + kQBytes, "merge area fits in the V and Q tiles");
     static_assert(kMaxClusterSplits * 64 * 4 <= kPBytes, "merge weights fit in the P tile");
-    if (p.splits < 1 || p.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
+    if (p.splits < 1 || p.splits > kMaxClusterSplits || (p.splits > 12 && p.splits < 16))
+        return cudaErrorInvalidValue;
+    if (p.splits > 8) cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     const size_t smem = 1024 + kVBytes + kQBytes + kPBytes + (8 * 64 + 3 * 64) * 4 +
                         kMaxClusterSplits * 2 * 64 * 4 + 9 * 8 + 64;
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

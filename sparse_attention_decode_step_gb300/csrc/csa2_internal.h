@@ -108,6 +108,8 @@ struct AttnParams {
 // Splits (CTAs, at most 8 = one cluster) per query, and the workspace (none).
 int attn_plan(int nq, int k_max, int n_win);
 size_t attn_workspace_bytes(int nq, int H, int k_max, int n_win);
+// The largest cluster of attention CTAs (splits of a query) this GPU schedules.
+int attn_max_splits();
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
 
 }  // namespace csa2

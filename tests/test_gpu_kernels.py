@@ -528,6 +528,21 @@ def test_attention_matches_oracle(H):
     assert c.tolist() == [0, 0, 0, 0]
 
 
+# (queries, rows per query) that make the planner divide a query over 2 .. 16
+# CTAs on a 152-SM GPU: the cluster merge at every size it uses, including
+# the sizes above the portable 8 and those whose owners take two chunk slots
+@pytest.mark.parametrize("nq,rows,splits", [(64, 2176, 2), (40, 2176, 3), (30, 2176, 5),
+                                            (21, 1792, 7), (19, 2048, 8), (15, 2560, 10),
+                                            (13, 1408, 11), (12, 1536, 12), (9, 2048, 16)])
+def test_attention_cluster_sizes(nq, rows, splits):
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _attn_splits(nq, rows) == splits
+    n_win = 128
+    cnts = [rows - n_win - (i % 3) * 40 for i in range(nq)]   # the first query has the most rows
+    c = _attn_case(64, 3000, cnts, n_win, 256, seed=nq)
+    assert c.tolist() == [0, 0, 0, 0]
+
+
 def test_attention_window_truncation_and_scale():
     _attn_case(64, 600, [300, 17], 128, 128, win_start=[560, 0], sm=0.37, seed=32)
 
@@ -564,11 +579,18 @@ def test_attention_more_queries_than_sms_single_split():
 LOG2E = 1.4426950408889634
 
 
-def _attn_splits(nq, n_rows_max):
-    """The number of CTAs per query the library uses (the rule of its planner)."""
+def _attn_splits(nq, n_rows_max, cap=16):
+    """The number of CTAs per query the library uses (the rule of its planner,
+    on a GPU that schedules clusters of 16): at most sms / nq, the tiles and
+    the cap, 13 .. 15 skipped, then as few as give the same tiles per split."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tiles = (n_rows_max + 127) // 128
-    return max(1, min(sms // nq, tiles, 8))
+    s = max(1, min(sms // nq, tiles, cap))
+    if 12 < s < 16:
+        s = 12
+    tps = (tiles + s - 1) // s
+    s = (tiles + tps - 1) // tps
+    return 16 if 12 < s < 16 else s
 
 
 def _split_tiles(n_rows, splits):
@@ -626,7 +648,7 @@ def test_attention_peaky_logits_rescale_and_split_merge(layout):
         for i in big:
             cnts[i] = 2048
     else:
-        # two queries split 8 ways: 8,000 + 128 rows (8 tiles per CTA) and 2,048 + 128
+        # two queries split 16 ways: 8,000 + 128 rows (4 tiles per CTA) and 2,048 + 128
         n_ent, nq = 12000, 2
         cnts = [8000, 2048]
         big = [0, 1]
@@ -648,7 +670,7 @@ def test_attention_peaky_logits_rescale_and_split_merge(layout):
             q[i] = rng.normal(size=(H, 512)) / np.sqrt(512.0)
     qa = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
     splits = _attn_splits(nq, k_max + n_win)
-    assert splits == (1 if layout == "one_split" else 8)
+    assert splits == (1 if layout == "one_split" else 16)
     # the inputs drive the paths under test (checked on exact logits)
     rescaled_late, far_apart = False, False
     for i in big:
