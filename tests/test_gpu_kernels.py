@@ -532,7 +532,8 @@ def test_attention_matches_oracle(H):
 # CTAs on a 152-SM GPU: the cluster merge at every size it uses, including
 # the sizes above the portable 8 and those whose owners take two chunk slots
 @pytest.mark.parametrize("nq,rows,splits", [(64, 2176, 2), (40, 2176, 3), (30, 2176, 5),
-                                            (21, 1792, 7), (19, 2048, 8), (15, 2560, 10),
+                                            (25, 2176, 6), (21, 1792, 7), (19, 2048, 8),
+                                            (15, 2560, 10),
                                             (13, 1408, 11), (12, 1536, 12), (9, 2048, 16)])
 def test_attention_cluster_sizes(nq, rows, splits):
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
