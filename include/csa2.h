@@ -253,8 +253,9 @@ csa2_status csa2_pool_select(const float *blockmax, int64_t ld_blockmax, const i
  * before normalisation, relative error 2^-11).  Logits, the softmax and every
  * sum are fp32.
  * The attention needs no workspace (csa2_attn_workspace_size() is 0; the
- * argument may be NULL): a query's row tiles are divided over at most 8 CTAs
- * of one thread-block cluster, which merge on chip. */
+ * argument may be NULL): a query's row tiles are divided over at most 16 CTAs
+ * of one thread-block cluster (8 where the GPU does not schedule clusters of
+ * 16), which merge on chip. */
 csa2_status csa2_sparse_attn(const csa2_cache *cache, const csa2_queries *queries,
                              const int32_t *idx, int64_t ld_idx, const int32_t *cnt,
                              int32_t k_max, const uint16_t *q, int32_t H, const uint16_t *win,
